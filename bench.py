@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Decode-step benchmark: the 197 NF4 GEMVs of one Qwen2.5-1.5B-shaped decode step at batch 1.
+
+One step = one replay of the step's CUDA graph (all 197 GEMVs, in order, each reading x only after
+the previous GEMV completed).  value = algorithmic HBM bytes of the step (packed weights + scales +
+x + y) / device time, in GB/s; the step's weights (871 MB) exceed the 129 MB L2, so no flush is
+needed between steps.  Rank 0 prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain float64 restatement of the method) on the same
+workload, a bounded row sample per step, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-step 4-bit GEMV µs and achieved HBM GB/s (% of GB300 roofline)"
+WORKLOAD = ("Qwen2.5-1.5B-shaped decode step, batch 1: 197 NF4 GEMVs (28 layers x q 1536x1536, "
+            "k 256x1536, v 256x1536, o 1536x1536, gate 8960x1536, up 8960x1536, down 1536x8960, "
+            "+ lm_head 151936x1536), blocksize 64, FP32 absmax, weights N(0,0.02), x N(0,1) FP16")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("w4_gemv.cu", "w4_common.cuh"):
+        h.update(open(os.path.join(ROOT, "weight_only_bit_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes of the GEMV kernel from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "gemv_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_sha") != kernel_sha():
+        return None
+    return d.get("dram_bytes_per_launch_full_step")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------- oracle timing
+def oracle_sample_rate(budget_s: float, fmt: str = "nf4"):
+    """The oracle (as it stands) on a row sample of the step's GEMVs, for about budget_s seconds.
+    Returns (GB/s of algorithmic bytes, cores, description)."""
+    import numpy as np
+    import oracle
+    from weight_only_bit_gb300 import synth
+    bs = 64 if fmt == "nf4" else 128
+    code = oracle.nf4_codebook()
+    pool = []
+    for proj in ("q", "k", "v", "o", "gate", "up", "down"):
+        n, k = synth.shape_of(proj)
+        rows = min(n, 512)
+        w = synth.weights(synth.weight_seed(0, proj), n, k)[:rows]
+        x = synth.activations(synth.x_seed(0, synth.X_SLOT[proj], 1), 1, k)
+        if fmt == "nf4":
+            p, s = oracle.quantize_nf4(w, code, bs)
+        else:
+            p, s = oracle.quantize_int4(w, bs)
+        sbytes = 4 if fmt == "nf4" else 2
+        nbytes = rows * k // 2 + rows * (k // bs) * sbytes + 2 * k + 2 * rows
+        pool.append((p, s, x, nbytes))
+    t0 = time.perf_counter()
+    done = 0
+    i = 0
+    while time.perf_counter() - t0 < budget_s:
+        p, s, x, nb = pool[i % len(pool)]
+        if fmt == "nf4":
+            oracle.gemv_nf4(p, s, code, x, bs)
+        else:
+            oracle.gemv_int4(p, s, x, bs)
+        done += nb
+        i += 1
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = (f"oracle.gemv_{fmt} (numpy float64 dequantise + BLAS matmul) over the first 512 rows of layer 0's "
+            f"seven projections, {i} GEMVs in {dt:.1f} s")
+    return done / dt / 1e9, cores, desc
+
+
+def run_reference(args):
+    """The oracle timed as the reference arm: each step a bounded row sample of the workload."""
+    import numpy as np
+    import oracle
+    from weight_only_bit_gb300 import synth
+    budget = float(os.environ.get("W4_REFERENCE_BUDGET_S", "60"))
+    per_step = budget / max(1, args.steps + args.warmup)
+    code = oracle.nf4_codebook()
+    shapes = [(proj,) + synth.shape_of(proj) for proj in ("q", "k", "v", "o", "gate", "up", "down", "lm_head")]
+    mats = {}
+    for proj, n, k in shapes:
+        rows = min(n, 256)
+        w = synth.weights(synth.weight_seed(28 if proj == "lm_head" else 0, proj), n, k)[:rows] \
+            if proj != "lm_head" else synth.weights(synth.weight_seed(28, proj), rows, k)
+        p, s = oracle.quantize_nf4(w, code, 64)
+        x = synth.activations(synth.x_seed(0, synth.X_SLOT[proj], 1), 1, k)
+        mats[proj] = (p, s, x, k)
+    # rows per step from a calibration call
+    p, s, x, k = mats["gate"]
+    t0 = time.perf_counter()
+    oracle.gemv_nf4(p, s, code, x, 64)
+    per_row = (time.perf_counter() - t0) / p.shape[0]
+    rows_per_step = max(1, min(256, int(per_step / max(per_row, 1e-9))))
+    order = [proj for _, proj, _, _ in synth.decode_step_gemvs()]
+    total_b, total_t = 0, 0.0
+    for it in range(args.warmup + args.steps):
+        proj = order[it % len(order)]
+        p, s, x, k = mats[proj]
+        r = min(rows_per_step, p.shape[0])
+        t0 = time.perf_counter()
+        oracle.gemv_nf4(p[:r], s[:r], code, x, 64)
+        dt = time.perf_counter() - t0
+        if it >= args.warmup:
+            total_t += dt
+            total_b += r * k // 2 + r * (k // 64) * 4 + 2 * k + 2 * r
+    gbs = total_b / total_t / 1e9
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"oracle.gemv_nf4 on {rows_per_step} rows per step of the step's GEMVs in order "
+              f"(float64 numpy), {args.steps} timed steps")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_t / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 1, "format": "nf4"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------- GPU arm
+def time_graph(step, stream, steps, warmup, torch):
+    for _ in range(warmup):
+        step.launch(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step.launch(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def per_shape(fmt, dev, torch, hbm):
+    """Each decode shape alone, batch 1: a graph of back-to-back launches of the same shape over
+    distinct weight copies totalling > 4x L2 (so every launch streams from HBM)."""
+    import weight_only_bit_gb300 as w4
+    from weight_only_bit_gb300 import synth
+    from weight_only_bit_gb300 import _lib
+    bs = 64 if fmt == "nf4" else 128
+    out = {}
+    code = None
+    if fmt == "nf4":
+        st, c = w4.w4_nf4_codebook()
+        code = torch.tensor(c, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    for name, n, k, _ in synth.DECODE_SHAPES:
+        w = synth.weights(synth.weight_seed(0 if name != "lm_head" else 28, name), n, k)
+        W = torch.from_numpy(w).to(dev)
+        packed = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
+        sdt = torch.float32 if fmt == "nf4" else torch.float16
+        sc = torch.empty((n, k // bs), dtype=sdt, device=dev)
+        if fmt == "nf4":
+            w4.check(w4.w4_quantize_nf4(W, packed, sc, code, n, k, bs))
+        else:
+            w4.check(w4.w4_quantize_int4(W, packed, sc, n, k, bs))
+        del W
+        per = n * k // 2 + sc.numel() * sc.element_size()
+        copies = max(2, min(4096, (4 * 129 * 2 ** 20) // per + 1))
+        P = packed.reshape(1, -1).repeat(copies, 1)
+        S = sc.reshape(1, -1).repeat(copies, 1)
+        x = torch.from_numpy(synth.activations(synth.x_seed(0, synth.X_SLOT[name], 1), 1, k)).to(dev)
+        y = torch.empty((1, n), dtype=torch.float16, device=dev)
+        descs = [dict(format=_lib.W4_FMT_NF4 if fmt == "nf4" else _lib.W4_FMT_INT4, packed=P[i], scales=S[i],
+                      codebook=code, x=x, y=y, M=1, N=n, K=k, blocksize=bs) for i in range(copies)]
+        st, h = w4.w4_step_create(descs)
+        w4.check(st, "per-shape graph")
+
+        class _G:
+            def launch(self, s):
+                return w4.w4_step_launch(h, s)
+        ms = time_graph(_G(), stream, 5, 2, torch) / copies
+        w4.w4_step_destroy(h)
+        nbytes = per + 2 * k + 2 * n
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"N": n, "K": k, "us": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
+                     "frac_of_measured": round(gbs / hbm, 4), "launches_timed": copies * 5}
+        del P, S
+    # the pages' "weighted" step: sum over shapes of count x per-launch time
+    weighted_us = sum(out[nm]["us"] * c for nm, _, _, c in synth.DECODE_SHAPES)
+    return out, weighted_us
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import weight_only_bit_gb300 as w4
+    from weight_only_bit_gb300 import build as _b
+    from weight_only_bit_gb300.step import DecodeStep
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+    if rank == 0 or world == 1:
+        _b.build()
+    if world > 1:
+        dist.barrier()
+    hbm, peak_src = peaks()
+
+    step = DecodeStep("nf4", batch=1, device=str(dev)).build().capture()
+    nbytes = step.bytes_per_step()
+    nlaunch = len(step.gemvs)
+    stream = torch.cuda.Stream(dev)
+
+    # warm-up, then the timed region bracketed by barrier + synchronize, clocks sampled inside
+    for _ in range(args.warmup):
+        step.launch(stream)
+    torch.cuda.synchronize()
+    w4.check(w4.w4_device_check(stream), "warm-up")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    l0 = w4.w4_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        w4.check(step.launch(stream))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = w4.w4_launch_count() - l0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    w4.check(w4.w4_device_check(stream), "timed region")
+    ms = e0.elapsed_time(e1) / args.steps
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    value = nbytes * world / (ms_max * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers: H2D of every x, the step, D2H of every y
+    x_pin = torch.from_numpy(step.x_host).pin_memory()
+    y_pin = torch.empty(step.y_elems, dtype=torch.float16).pin_memory()
+    e2e_steps = max(20, args.steps // 10)
+    for _ in range(3):
+        step.x.copy_(x_pin, non_blocking=True)
+        step.launch(stream)
+        y_pin.copy_(step.y, non_blocking=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(e2e_steps):
+            step.x.copy_(x_pin, non_blocking=True)
+            w4.check(step.launch(stream))
+            y_pin.copy_(step.y, non_blocking=True)
+        f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / e2e_steps
+    e2e = {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": int(step.x_elems * 2), "d2h_bytes_per_step": int(step.y_elems * 2),
+           "ms_per_step": round(e2e_ms, 5)}
+    step.close()
+
+    extra = {}
+    if rank == 0 and not args.quick:
+        # INT4 step (same shapes) and each shape alone
+        s4 = DecodeStep("int4", batch=1, device=str(dev)).build().capture()
+        ms4 = time_graph(s4, stream, max(100, args.steps // 4), args.warmup, torch)
+        b4 = s4.bytes_per_step()
+        extra["int4_step"] = {"us": round(ms4 * 1e3, 2), "GB_s": round(b4 / (ms4 * 1e-3) / 1e9, 1),
+                              "frac_of_measured": round(b4 / (ms4 * 1e-3) / 1e9 / hbm, 4), "bytes": b4}
+        s4.close()
+        del s4
+        torch.cuda.empty_cache()
+        shapes, weighted = per_shape("nf4", dev, torch, hbm)
+        extra["per_shape_nf4"] = shapes
+        extra["weighted_step_us_nf4"] = round(weighted, 2)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs_cpu, cores, desc = oracle_sample_rate(float(os.environ.get("W4_CPU_BASELINE_S", "12")))
+        cpu = {"value": round(gbs_cpu, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        achieved = (nbytes / nlaunch) / (ms_max * 1e-3 / nlaunch) / 1e9
+        traffic = ncu_traffic()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "us_per_step": round(ms_max * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": 1, "format": "nf4", "gemvs": nlaunch,
+                       "bytes_per_step": nbytes, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "no flush: 871 MB of distinct weights per step > 129 MB L2",
+                       "launch": "one CUDA graph per step, programmatic dependent launch"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "traffic": traffic,
+                         "peak_source": peak_src, "kernel": "gemv_simt_kernel<NF4,1> (all 197 launches)"},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
+            "frac_of_nominal_8TBs": round(value / world / 8000.0, 4),
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="skip the INT4 step and the per-shape table")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

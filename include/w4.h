@@ -1,0 +1,179 @@
+/*
+ * w4.h -- C ABI of libw4: fused 4-bit weight-only dequant-GEMV (W4A16) for GB300 (sm_103a).
+ *
+ * Formats
+ *   NF4  ("LLM Quantization on RTX 4060: Where 4-bit Decode Falls Behind FP16",
+ *         section "Standard Expectation from Quantization"): a 16-entry normal-float code
+ *         book, blocks of `blocksize` (default 64) consecutive weights of one row share one
+ *         FP32 absmax, two 4-bit codes per byte.
+ *   INT4 ("My Triton Kernel Ties bitsandbytes -- and Both Lose to Math", section "The kernels":
+ *         the +8 zero point; group size 128 as in "LLM Compressor 0.14: GPTQ's 15x speedup is
+ *         one fused loop", section "How the 15x and 30x were measured"): groups of `group`
+ *         weights of one row share one FP16 scale = absmax / 7; the nibble holds q + 8.
+ *
+ * Layouts (row-major, "out x in" = N x K, as the fused kernel of the first page indexes them,
+ * section "Kernel Implementation")
+ *   packed  uint8  [N][K/2]   byte j of a row = (code of element 2j) << 4 | code of element 2j+1
+ *   absmax  float  [N][K/blocksize]            (NF4)
+ *   scale   fp16   [N][K/group]                (INT4; IEEE binary16 bits in uint16_t)
+ *   codebook float [16], ascending             (NF4)
+ *   x       fp16   [M][K]   activations, M = batch (1 ... 128)
+ *   y       fp16   [M][N]   y[m][n] = sum_k w_hat[n][k] * x[m][k], accumulated in FP32
+ *
+ * Ownership and execution
+ *   Every pointer is a device pointer owned by the caller (except w4_nf4_codebook's output and
+ *   the descriptor array of w4_gemv_sequence / w4_step_create, which are host memory).  No call
+ *   allocates device memory on its launch path, none synchronises the device, and every launch
+ *   goes to the given stream (NULL = legacy default stream).  y is overwritten completely: no
+ *   pre-zeroing, no accumulation into y, repeated calls give identical bits.
+ *
+ *   GEMV kernels use programmatic dependent launch: a GEMV may start while the kernel before it
+ *   in the stream is finishing, and it reads packed weights, scales and the code book before that
+ *   kernel has completed; it reads x and writes y only after.  So weights, scales and code book
+ *   must not be produced by the kernel that immediately precedes the GEMV in the same stream if
+ *   that kernel signals early launch (only libw4's own GEMV kernels do, and they write only y).
+ *
+ * Errors
+ *   Every call validates its arguments on the host before touching CUDA and returns a w4_status.
+ *   W4_ERR_CUDA means a CUDA runtime call failed; w4_last_cuda_error() returns its cudaError_t.
+ *   Device-side waits are bounded; a wait that runs out sets a device error word that
+ *   w4_device_check() reads (it synchronises the stream) and reports as W4_ERR_TIMEOUT.
+ */
+#ifndef W4_H
+#define W4_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t (struct CUstream_st*); declared here so that the header needs
+ * no CUDA include. */
+typedef struct CUstream_st* w4_stream_t;
+
+typedef enum {
+  W4_OK = 0,
+  W4_ERR_NULL = -1,        /* a required pointer is NULL                                   */
+  W4_ERR_SHAPE = -2,       /* M, N or K out of range; K not a multiple of the block size    */
+  W4_ERR_ALIGN = -3,       /* a device pointer breaks the alignment its call states          */
+  W4_ERR_BLOCKSIZE = -4,   /* block / group size is not a power of two in [32, 256]          */
+  W4_ERR_CUDA = -5,        /* a CUDA runtime call failed; see w4_last_cuda_error()          */
+  W4_ERR_TIMEOUT = -6,     /* a bounded device-side wait ran out (reported by w4_device_check) */
+  W4_ERR_UNSUPPORTED = -7  /* valid arguments outside what this build implements           */
+} w4_status;
+
+typedef enum { W4_FMT_NF4 = 0, W4_FMT_INT4 = 1 } w4_format;
+
+/* Limits of this build. */
+#define W4_MAX_BATCH 128        /* M; prefill-sized GEMMs are not served                      */
+#define W4_MAX_K 10240          /* K; one consumer thread per 32-weight chunk of a row         */
+
+/* ---------------------------------------------------------------------------------------
+ * w4_nf4_codebook -- the 16 NF4 code values, ascending, FP32 (host function, no CUDA).
+ * The pages name the standard NF4 code book without printing it; this is the QLoRA
+ * construction ("4-bit NormalFloat", Dettmers et al. 2023): normal quantiles at
+ * probabilities evenly spaced from delta = ((1 - 1/32) + (1 - 1/30)) / 2 down to 1/2, eight
+ * on the positive side and seven on the negative side, an exact zero, all divided by the
+ * largest; float64 arithmetic, one rounding to FP32.  Result: out[0] = -1, out[7] = 0,
+ * out[15] = 1.  Returns W4_ERR_NULL if out is NULL.
+ */
+int w4_nf4_codebook(float out[16]);
+
+/* ---------------------------------------------------------------------------------------
+ * w4_quantize_nf4 -- block-wise NF4 quantisation of an FP32 matrix W [N][K] (device).
+ * Per block of `blocksize` weights of a row: a = max |w| -> absmax; n = w / a (IEEE FP32
+ * division; a == 0 gives n = 0); code = the nearest code-book value to n, a tie going to the
+ * lower code (decided exactly: n is compared with the midpoints (c[i] + c[i+1]) / 2 in
+ * float64); two codes per byte, element 2j in the high nibble ("LLM Quantization on RTX 4060",
+ * sections "Standard Expectation from Quantization" and "Kernel Implementation").
+ * codebook must be ascending.  W entries must be finite.
+ * Sizes: N >= 1, blocksize <= K <= W4_MAX_K, K % blocksize == 0, blocksize a power of two in
+ * [32, 256].  W, packed, absmax 16-byte aligned.  The same size rules hold for every call below.
+ */
+int w4_quantize_nf4(const float* W, uint8_t* packed, float* absmax, const float* codebook,
+                    int N, int K, int blocksize, w4_stream_t stream);
+
+/* w4_quantize_int4 -- group-wise INT4 with the +8 zero point ("My Triton Kernel Ties
+ * bitsandbytes", section "The kernels").  Per group: s = fp16(absmax / 7) (the FP32 quotient
+ * rounded to FP16); q = clamp(rint(w / s), -8, 7) + 8 with w / s an IEEE FP32 division and
+ * rint rounding halves to even ("LLM Compressor 0.14", section "Details worth knowing");
+ * s == 0 gives q = 8.  |w| must stay below 7 * 65504 (so that s is finite). */
+int w4_quantize_int4(const float* W, uint8_t* packed, uint16_t* scale,
+                     int N, int K, int group, w4_stream_t stream);
+
+/* w4_dequantize_nf4 -- W_out[n][k] = code[q] * absmax (FP32 product), a test and
+ * debugging aid; the GEMVs never materialise this matrix.  W_out 8-byte aligned. */
+int w4_dequantize_nf4(const uint8_t* packed, const float* absmax, const float* codebook,
+                      float* W_out, int N, int K, int blocksize, w4_stream_t stream);
+
+/* w4_dequantize_int4 -- W_out[n][k] = (q - 8) * s, exact in FP32. */
+int w4_dequantize_int4(const uint8_t* packed, const uint16_t* scale, float* W_out,
+                       int N, int K, int group, w4_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * w4_gemv_nf4 / w4_gemv_int4 -- y = x . dequant(W)^T in one pass: packed weights and scales
+ * are streamed once, unpacked and decoded on chip and accumulated in FP32 against x; no
+ * dequantised weight matrix is ever written ("LLM Quantization on RTX 4060", sections
+ * "Fused Kernel: Moving Dequantization On-Chip" and "Kernel Implementation"; FP32
+ * accumulation as that kernel's comment requires).  y is rounded to FP16 (nearest even).
+ * Batches 1 ... 31 run on CUDA cores; batches 32 ... 128 on the tensor cores.
+ * Sizes: 1 <= M <= W4_MAX_BATCH, N >= 1, 32 <= K <= W4_MAX_K, K % blocksize == 0,
+ * blocksize a power of two in [32, 256].  packed, scales, x 16-byte aligned; y 2-byte aligned.
+ * Agreement with the float64 definition: relative L2 error <= 1e-3 and
+ * max |error| <= 2e-2 * RMS(y) per output vector.
+ */
+int w4_gemv_nf4(const uint8_t* packed, const float* absmax, const float* codebook,
+                const uint16_t* x, uint16_t* y, int M, int N, int K, int blocksize,
+                w4_stream_t stream);
+int w4_gemv_int4(const uint8_t* packed, const uint16_t* scale,
+                 const uint16_t* x, uint16_t* y, int M, int N, int K, int group,
+                 w4_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Decode step: the projections of one decode step launched back to back ("Do Quantization and
+ * Sparsity make LLM Inference Faster ?", section "What we did": 197 GEMVs per token), each
+ * GEMV reading x only after every earlier GEMV of the sequence has completed.
+ */
+typedef struct {
+  int format;               /* w4_format                                               */
+  const uint8_t* packed;    /* [N][K/2]                                                 */
+  const void* scales;       /* float absmax [N][K/bs] (NF4) or fp16 scale [N][K/gs] (INT4) */
+  const float* codebook;    /* [16] for NF4, ignored for INT4                           */
+  const uint16_t* x;        /* [M][K] fp16                                              */
+  uint16_t* y;              /* [M][N] fp16                                              */
+  int M, N, K, blocksize;
+} w4_gemv_desc;
+
+/* Validates every descriptor, then enqueues the GEMVs in order on `stream`. */
+int w4_gemv_sequence(const w4_gemv_desc* descs, int count, w4_stream_t stream);
+
+/* A decode step captured once into a CUDA graph.  w4_step_create validates, captures the
+ * sequence on a private stream and instantiates the graph (host-side objects only; no device
+ * buffers are allocated); w4_step_launch replays it on `stream`.  The descriptors' pointers are
+ * baked into the graph: the buffers must outlive the step. */
+typedef struct w4_step w4_step;
+int w4_step_create(const w4_gemv_desc* descs, int count, w4_step** out);
+int w4_step_launch(w4_step* step, w4_stream_t stream);
+int w4_step_destroy(w4_step* step);
+
+/* ---------------------------------------------------------------------------------------
+ * Diagnostics. */
+const char* w4_status_str(int status);
+int w4_last_cuda_error(void);          /* cudaError_t of the last W4_ERR_CUDA in this thread */
+/* Synchronises `stream`, reads and clears the device error word of the current device:
+ * W4_OK, or W4_ERR_TIMEOUT if a bounded device-side wait ran out since the last check. */
+int w4_device_check(w4_stream_t stream);
+/* Kernel launches the library has issued in this process (for launch accounting). */
+long long w4_launch_count(void);
+
+/* Test hook for the timeout path.  The next CUDA-core GEMV launch in this process has its
+ * producer warp issue no copies, so every consumer's bounded wait (one second) runs out; the
+ * kernel records the failure and returns without faulting, its output is garbage, and the next
+ * w4_device_check() returns W4_ERR_TIMEOUT.  The context stays usable.  Returns W4_OK. */
+int w4_inject_timeout_once(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4_H */

@@ -8,3 +8,15 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built libw4")
+
+
+import pytest
+
+
+@pytest.fixture(scope="session")
+def libw4():
+    """Builds libw4.so in-tree if it is missing or stale (nvcc cross-compiles without a GPU)."""
+    from weight_only_bit_gb300 import build as _b
+    _b.build()
+    from weight_only_bit_gb300._lib import lib
+    return lib()

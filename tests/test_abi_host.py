@@ -1,0 +1,95 @@
+"""The C ABI on the host: the library loads without a GPU, exports every symbol include/w4.h
+declares, validates arguments before touching CUDA, and its host-side code book matches the
+oracle's construction bit for bit."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import weight_only_bit_gb300 as w4
+from weight_only_bit_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "w4.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(_lib.SYMBOLS) == _declared()
+
+
+def test_every_declared_symbol_is_exported(libw4):
+    for name in _declared():
+        assert hasattr(libw4, name), name
+
+
+def test_codebook_matches_oracle_bit_for_bit(libw4):
+    st, c = w4.w4_nf4_codebook()
+    assert st == w4.W4_OK if hasattr(w4, "W4_OK") else st == 0
+    lib_c = np.array(c, dtype=np.float32)
+    assert np.array_equal(lib_c.view(np.uint32), oracle.nf4_codebook().view(np.uint32))
+    assert libw4.w4_nf4_codebook(None) == _lib.W4_ERR_NULL
+
+
+# fake, never dereferenced device addresses (validation returns before any CUDA call)
+A = 1 << 20
+
+
+def test_gemv_validation(libw4):
+    g = libw4.w4_gemv_nf4
+    ok = (A, A, A, A, A)
+    assert g(None, A, A, A, A, 1, 256, 1536, 64, None) == _lib.W4_ERR_NULL
+    assert g(A, A, None, A, A, 1, 256, 1536, 64, None) == _lib.W4_ERR_NULL          # NF4 needs a code book
+    assert g(*ok, 1, 256, 1536, 48, None) == _lib.W4_ERR_BLOCKSIZE                  # not a power of two
+    assert g(*ok, 1, 256, 1536, 16, None) == _lib.W4_ERR_BLOCKSIZE                  # below 32
+    assert g(*ok, 1, 256, 1536, 512, None) == _lib.W4_ERR_BLOCKSIZE                 # above 256
+    assert g(*ok, 1, 256, 1568, 64, None) == _lib.W4_ERR_SHAPE                      # K % bs != 0
+    assert g(*ok, 0, 256, 1536, 64, None) == _lib.W4_ERR_SHAPE                      # empty batch
+    assert g(*ok, 1, 0, 1536, 64, None) == _lib.W4_ERR_SHAPE                        # empty output
+    assert g(*ok, 129, 256, 1536, 64, None) == _lib.W4_ERR_UNSUPPORTED              # beyond the batch limit
+    assert g(*ok, 1, 256, _lib.W4_MAX_K + 64, 64, None) == _lib.W4_ERR_UNSUPPORTED  # beyond the K limit
+    assert g(A + 8, A, A, A, A, 1, 256, 1536, 64, None) == _lib.W4_ERR_ALIGN          # packed
+    assert g(A, A + 4, A, A, A, 1, 256, 1536, 64, None) == _lib.W4_ERR_ALIGN          # absmax
+    assert g(A, A, A, A + 2, A, 1, 256, 1536, 64, None) == _lib.W4_ERR_ALIGN          # x
+    assert g(A, A, A, A, A + 1, 1, 256, 1536, 64, None) == _lib.W4_ERR_ALIGN          # y (2-byte rule)
+    gi = libw4.w4_gemv_int4
+    assert gi(A, None, A, A, 1, 256, 1536, 128, None) == _lib.W4_ERR_NULL
+    assert gi(A, A, A, A, 1, 256, 1536, 96, None) == _lib.W4_ERR_BLOCKSIZE
+
+
+def test_quantize_and_dequantize_validation(libw4):
+    assert libw4.w4_quantize_nf4(None, A, A, A, 4, 64, 64, None) == _lib.W4_ERR_NULL
+    assert libw4.w4_quantize_nf4(A, A, A, A, 4, 100, 64, None) == _lib.W4_ERR_SHAPE
+    assert libw4.w4_quantize_nf4(A + 4, A, A, A, 4, 64, 64, None) == _lib.W4_ERR_ALIGN
+    assert libw4.w4_quantize_int4(A, A, A, 4, 128, 100, None) == _lib.W4_ERR_BLOCKSIZE
+    assert libw4.w4_dequantize_nf4(A, A, A, None, 4, 64, 64, None) == _lib.W4_ERR_NULL
+    assert libw4.w4_dequantize_int4(A, A, A + 4, 4, 128, 128, None) == _lib.W4_ERR_ALIGN
+
+
+def test_sequence_and_step_validation(libw4):
+    d = (_lib.GemvDesc * 2)()
+    d[0] = _lib.GemvDesc(_lib.W4_FMT_NF4, A, A, A, A, A, 1, 256, 1536, 64)
+    d[1] = _lib.GemvDesc(_lib.W4_FMT_INT4, A, A, 0, A, A, 1, 256, 1536, 100)   # bad group
+    assert libw4.w4_gemv_sequence(d, 2, None) == _lib.W4_ERR_BLOCKSIZE           # nothing enqueued
+    assert libw4.w4_gemv_sequence(None, 2, None) == _lib.W4_ERR_NULL
+    h = ctypes.c_void_p()
+    assert libw4.w4_step_create(d, 2, ctypes.byref(h)) == _lib.W4_ERR_BLOCKSIZE and h.value is None
+    assert libw4.w4_step_launch(None, None) == _lib.W4_ERR_NULL
+    assert libw4.w4_step_destroy(None) == _lib.W4_ERR_NULL
+    d[0].format = 7
+    assert libw4.w4_gemv_sequence(d, 1, None) == _lib.W4_ERR_UNSUPPORTED
+
+
+def test_status_strings(libw4):
+    for code in range(-7, 1):
+        assert libw4.w4_status_str(code)
+    assert w4.w4_status_str(_lib.W4_ERR_ALIGN) != w4.w4_status_str(_lib.W4_ERR_SHAPE)
+    with pytest.raises(w4.W4Error):
+        w4.check(_lib.W4_ERR_SHAPE, "shape")

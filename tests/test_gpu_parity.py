@@ -1,0 +1,271 @@
+"""CUDA path against the oracle, through the C ABI, on seeded synthetic inputs.
+
+Bars (from the target's stated criteria):
+  * packing, codes, absmax, FP16 scales and dequantised weights: bit-exact;
+  * GEMV: per output vector, relative L2 error <= 1e-3 and max |error| <= 2e-2 * RMS(y_ref)
+    against the float64 oracle.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import weight_only_bit_gb300 as w4
+from weight_only_bit_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-3
+MAX_ABS_RMS = 2e-2
+
+
+@pytest.fixture(scope="module")
+def dev(libw4):
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    return torch.device("cuda:0")
+
+
+def _t(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def _code(dev):
+    return _t(oracle.nf4_codebook(), dev)
+
+
+def gpu_quantize(fmt, w, bs, dev):
+    n, k = w.shape
+    W = _t(w, dev)
+    packed = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
+    if fmt == "nf4":
+        sc = torch.empty((n, k // bs), dtype=torch.float32, device=dev)
+        w4.check(w4.w4_quantize_nf4(W, packed, sc, _code(dev), n, k, bs))
+    else:
+        sc = torch.empty((n, k // bs), dtype=torch.float16, device=dev)
+        w4.check(w4.w4_quantize_int4(W, packed, sc, n, k, bs))
+    return packed, sc
+
+
+def gpu_gemv(fmt, packed, sc, x, n, k, bs, dev, y=None):
+    m = x.shape[0]
+    X = _t(x, dev)
+    if y is None:
+        y = torch.full((m, n), float("nan"), dtype=torch.float16, device=dev)
+    if fmt == "nf4":
+        w4.check(w4.w4_gemv_nf4(packed, sc, _code(dev), X, y, m, n, k, bs))
+    else:
+        w4.check(w4.w4_gemv_int4(packed, sc, X, y, m, n, k, bs))
+    torch.cuda.synchronize()
+    return y
+
+
+def oracle_quantize(fmt, w, bs):
+    if fmt == "nf4":
+        return oracle.quantize_nf4(w, oracle.nf4_codebook(), bs)
+    return oracle.quantize_int4(w, bs)
+
+
+def oracle_gemv(fmt, packed, sc, x, bs, rows=None):
+    if fmt == "nf4":
+        return oracle.gemv_nf4(packed, sc, oracle.nf4_codebook(), x, bs, rows=rows)
+    return oracle.gemv_int4(packed, sc, x, bs, rows=rows)
+
+
+def assert_gemv_close(y, y_ref):
+    y = np.asarray(y, dtype=np.float64)
+    assert np.all(np.isfinite(y))
+    for m in range(y_ref.shape[0]):
+        err = y[m] - y_ref[m]
+        rms = np.sqrt(np.mean(y_ref[m] ** 2))
+        rel = np.linalg.norm(err) / max(np.linalg.norm(y_ref[m]), 1e-300)
+        assert rel <= REL_L2, f"row {m}: relative L2 {rel:.3e}"
+        assert np.max(np.abs(err)) <= MAX_ABS_RMS * rms, f"row {m}: max abs {np.max(np.abs(err)):.3e} rms {rms:.3e}"
+
+
+QUANT_CASES = [
+    # (fmt, N, K, bs)
+    ("nf4", 1, 64, 64), ("nf4", 3, 128, 64), ("nf4", 257, 1536, 64), ("nf4", 16, 8960, 64),
+    ("nf4", 5, 256, 32), ("nf4", 7, 512, 128), ("nf4", 2, 512, 256),
+    ("int4", 1, 128, 128), ("int4", 3, 256, 128), ("int4", 257, 1536, 128), ("int4", 16, 8960, 128),
+    ("int4", 5, 256, 32), ("int4", 7, 512, 64), ("int4", 2, 512, 256),
+]
+
+
+@pytest.mark.parametrize("fmt,n,k,bs", QUANT_CASES)
+def test_quantize_bit_exact(dev, fmt, n, k, bs):
+    w = synth.weights(1000 + n + k + bs, n, k, outlier_frac=0.01)
+    w[0, : min(k, bs)] = 0.0                                   # an all-zero block
+    packed, sc = gpu_quantize(fmt, w, bs, dev)
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    assert np.array_equal(packed.cpu().numpy(), p_ref)
+    got = sc.cpu().numpy()
+    assert got.dtype == s_ref.dtype and np.array_equal(got.view(np.uint8), s_ref.view(np.uint8))
+
+
+@pytest.mark.parametrize("fmt,bs", [("nf4", 64), ("int4", 128)])
+def test_quantize_ties_and_grid_points(dev, fmt, bs):
+    """Values exactly on code points and exactly at rounding boundaries."""
+    code = oracle.nf4_codebook()
+    rows = []
+    if fmt == "nf4":
+        a = np.float32(2.0 ** -5)
+        q = np.arange(64) % 16
+        rows.append((code[q] * a).astype(np.float32))
+        mids = ((code[:-1].astype(np.float64) + code[1:]) / 2 * float(a)).astype(np.float32)
+        r = np.zeros(64, np.float32); r[:15] = mids; r[15] = a
+        rows.append(r)
+    else:
+        s = 2.0 ** -6
+        t = np.array([2.5, 3.5, -2.5, -3.5, 0.5, -0.5, 1.5, 6.5, -6.5], np.float64)
+        r = np.zeros(128, np.float32); r[: len(t)] = (t * s).astype(np.float32); r[127] = 7 * s
+        rows.append(r)
+        rows.append(((np.arange(128) % 15 - 7) * s).astype(np.float32))
+    w = np.stack(rows)
+    packed, sc = gpu_quantize(fmt, w, bs, dev)
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    assert np.array_equal(packed.cpu().numpy(), p_ref)
+    assert np.array_equal(sc.cpu().numpy().view(np.uint8), s_ref.view(np.uint8))
+
+
+@pytest.mark.parametrize("fmt,n,k,bs", [c for c in QUANT_CASES if c[1] > 1])
+def test_dequantize_bit_exact(dev, fmt, n, k, bs):
+    w = synth.weights(2000 + n + k, n, k)
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    packed, sc = _t(p_ref, dev), _t(s_ref, dev)
+    out = torch.empty((n, k), dtype=torch.float32, device=dev)
+    if fmt == "nf4":
+        w4.check(w4.w4_dequantize_nf4(packed, sc, _code(dev), out, n, k, bs))
+        ref = oracle.dequantize_nf4(p_ref, s_ref, oracle.nf4_codebook(), bs)
+    else:
+        w4.check(w4.w4_dequantize_int4(packed, sc, out, n, k, bs))
+        ref = oracle.dequantize_int4(p_ref, s_ref, bs)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+GEMV_CASES = [
+    # (fmt, M, N, K, bs): tiny, ragged, several tiles, both K of the decode step
+    ("nf4", 1, 1, 64, 64), ("nf4", 1, 3, 128, 64), ("nf4", 1, 257, 1536, 64), ("nf4", 1, 256, 1536, 64),
+    ("nf4", 1, 1536, 1536, 64), ("nf4", 1, 100, 8960, 64), ("nf4", 2, 333, 1536, 64), ("nf4", 3, 64, 8960, 64),
+    ("nf4", 4, 1000, 1536, 64), ("nf4", 5, 129, 1536, 64), ("nf4", 8, 777, 1536, 64), ("nf4", 8, 61, 8960, 64),
+    ("nf4", 1, 70, 512, 32), ("nf4", 1, 70, 512, 128), ("nf4", 2, 70, 1024, 256),
+    ("int4", 1, 1, 128, 128), ("int4", 1, 3, 256, 128), ("int4", 1, 257, 1536, 128), ("int4", 1, 256, 1536, 128),
+    ("int4", 1, 1536, 1536, 128), ("int4", 1, 100, 8960, 128), ("int4", 2, 333, 1536, 128), ("int4", 3, 64, 8960, 128),
+    ("int4", 4, 1000, 1536, 128), ("int4", 5, 129, 1536, 128), ("int4", 8, 777, 1536, 128), ("int4", 8, 61, 8960, 128),
+    ("int4", 1, 70, 512, 32), ("int4", 1, 70, 512, 64), ("int4", 2, 70, 1024, 256),
+]
+
+
+@pytest.mark.parametrize("fmt,m,n,k,bs", GEMV_CASES)
+def test_gemv_parity(dev, fmt, m, n, k, bs):
+    w = synth.weights(3000 + n + k + m, n, k, outlier_frac=0.001)
+    x = synth.activations(4000 + n + k + m, m, k)
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    y = gpu_gemv(fmt, _t(p_ref, dev), _t(s_ref, dev), x, n, k, bs, dev)
+    assert_gemv_close(y.cpu().numpy(), oracle_gemv(fmt, p_ref, s_ref, x, bs))
+
+
+@pytest.mark.parametrize("fmt", ["nf4", "int4"])
+@pytest.mark.parametrize("m", [12, 20, 32, 64, 128])
+def test_gemv_parity_larger_batches(dev, fmt, m):
+    bs = 64 if fmt == "nf4" else 128
+    n, k = 300, 1536
+    w = synth.weights(5000 + m, n, k)
+    x = synth.activations(5100 + m, m, k)
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    y = gpu_gemv(fmt, _t(p_ref, dev), _t(s_ref, dev), x, n, k, bs, dev)
+    assert_gemv_close(y.cpu().numpy(), oracle_gemv(fmt, p_ref, s_ref, x, bs))
+
+
+@pytest.mark.parametrize("fmt", ["nf4", "int4"])
+def test_gemv_one_hot_zero_linearity_idempotence(dev, fmt):
+    bs = 64 if fmt == "nf4" else 128
+    n, k = 96, 1536
+    w = synth.weights(6000, n, k)
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    packed, sc = _t(p_ref, dev), _t(s_ref, dev)
+    wh = oracle.dequantize_nf4(p_ref, s_ref, oracle.nf4_codebook(), bs) if fmt == "nf4" else \
+        oracle.dequantize_int4(p_ref, s_ref, bs)
+    # one-hot x picks column k of w_hat: pins nibble order, block index and orientation
+    for kk in (0, 1, 63, 64, 1535):
+        x = np.zeros((1, k), np.float16)
+        x[0, kk] = 1.0
+        y = gpu_gemv(fmt, packed, sc, x, n, k, bs, dev).cpu().numpy()[0]
+        exp = wh[:, kk].astype(np.float16)
+        if fmt == "int4":
+            assert np.array_equal(y.view(np.uint16), exp.view(np.uint16))        # exact path
+        else:
+            assert np.allclose(y.astype(np.float64), wh[:, kk], rtol=2 ** -10, atol=0)
+    # zero input gives exactly zero
+    y0 = gpu_gemv(fmt, packed, sc, np.zeros((2, k), np.float16), n, k, bs, dev).cpu().numpy()
+    assert np.all(y0 == 0)
+    # linearity: doubling x doubles y bit for bit (power-of-two scaling commutes with rounding)
+    x = synth.activations(6100, 2, k)
+    y1 = gpu_gemv(fmt, packed, sc, x, n, k, bs, dev).cpu().numpy()
+    y2 = gpu_gemv(fmt, packed, sc, (2 * x.astype(np.float32)).astype(np.float16), n, k, bs, dev).cpu().numpy()
+    assert np.array_equal((2 * y1.astype(np.float32)).astype(np.float16).view(np.uint16), y2.view(np.uint16))
+    # idempotence: a second launch into the same (dirty) y gives identical bits
+    X = _t(x, dev)
+    ya = torch.full((2, n), 7.0, dtype=torch.float16, device=dev)
+    for _ in range(2):
+        if fmt == "nf4":
+            w4.check(w4.w4_gemv_nf4(packed, sc, _code(dev), X, ya, 2, n, k, bs))
+        else:
+            w4.check(w4.w4_gemv_int4(packed, sc, X, ya, 2, n, k, bs))
+        torch.cuda.synchronize()
+        assert np.array_equal(ya.cpu().numpy().view(np.uint16), y1.view(np.uint16))
+
+
+@pytest.mark.parametrize("fmt", ["nf4", "int4"])
+def test_gemv_writes_nothing_outside_y(dev, fmt):
+    bs = 64 if fmt == "nf4" else 128
+    n, k, m = 131, 1536, 3
+    w = synth.weights(7000, n, k)
+    x = synth.activations(7001, m, k)
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    guard = 2048
+    buf = torch.full((guard + m * n + guard,), 1234.0, dtype=torch.float16, device=dev)
+    y = buf[guard: guard + m * n].view(m, n)
+    gpu_gemv(fmt, _t(p_ref, dev), _t(s_ref, dev), x, n, k, bs, dev, y=y)
+    b = buf.cpu().numpy()
+    assert np.all(b[:guard] == 1234.0) and np.all(b[guard + m * n:] == 1234.0)
+    assert_gemv_close(y.cpu().numpy(), oracle_gemv(fmt, p_ref, s_ref, x, bs))
+
+
+@pytest.mark.parametrize("fmt", ["nf4", "int4"])
+def test_decode_shapes_full_size_sampled(dev, fmt):
+    """Every decode-step shape at full size, quantised on the GPU; sampled output rows checked
+    one by one against the oracle (which quantises those rows itself)."""
+    bs = 64 if fmt == "nf4" else 128
+    rng = np.random.default_rng(8)
+    for name, n, k, _ in synth.DECODE_SHAPES:
+        w = synth.weights(synth.weight_seed(0 if name != "lm_head" else 28, name), n, k)
+        x = synth.activations(synth.x_seed(0, synth.X_SLOT[name], 1), 1, k)
+        packed, sc = gpu_quantize(fmt, w, bs, dev)
+        y = gpu_gemv(fmt, packed, sc, x, n, k, bs, dev).cpu().numpy()
+        rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 64)]))
+        p_ref, s_ref = oracle_quantize(fmt, w[rows], bs)
+        assert np.array_equal(packed.cpu().numpy()[rows], p_ref)
+        y_ref = oracle_gemv(fmt, p_ref, s_ref, x, bs)
+        err = y[0, rows].astype(np.float64) - y_ref[0]
+        # per-element bound of the criteria (the RMS over the sampled rows)
+        rms = np.sqrt(np.mean(y_ref[0] ** 2))
+        assert np.max(np.abs(err)) <= MAX_ABS_RMS * rms, name
+        assert np.linalg.norm(err) <= REL_L2 * np.linalg.norm(y_ref[0]), name
+
+
+def test_timeout_is_reported_and_context_survives(dev):
+    """A producer that issues nothing (host-set test hook) makes every bounded wait run out after
+    about a second; the kernel returns, the host reads W4_ERR_TIMEOUT, and the next GEMV is right."""
+    n, k, bs = 64, 1536, 64
+    w = synth.weights(9000, n, k)
+    x = synth.activations(9001, 1, k)
+    p_ref, s_ref = oracle_quantize("nf4", w, bs)
+    packed, sc = _t(p_ref, dev), _t(s_ref, dev)
+    assert w4.w4_device_check() == 0
+    w4.w4_inject_timeout_once()
+    gpu_gemv("nf4", packed, sc, x, n, k, bs, dev)
+    assert w4.w4_device_check() == w4._lib.W4_ERR_TIMEOUT
+    assert w4.w4_device_check() == 0                      # cleared after reading
+    y = gpu_gemv("nf4", packed, sc, x, n, k, bs, dev)
+    assert_gemv_close(y.cpu().numpy(), oracle_gemv("nf4", p_ref, s_ref, x, bs))

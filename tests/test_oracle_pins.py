@@ -322,5 +322,8 @@ def test_synth_is_seeded_and_shaped():
     assert a.dtype == np.float32 and a.shape == (8, 64) and np.array_equal(a, b)
     o = synth.weights(12, 100, 100, outlier_frac=0.001)
     assert np.sum(np.abs(o) == np.float32(0.2)) == 10
+    big = synth.weights(14, 2500, 64, outlier_frac=0.001)       # three row blocks
+    rows = [0, 1023, 1024, 2499, 7]
+    assert np.array_equal(synth.weights_rows(14, 2500, 64, rows, outlier_frac=0.001), big[rows])
     x = synth.activations(13, 2, 64)
     assert x.dtype == np.float16 and x.shape == (2, 64)

@@ -1,0 +1,291 @@
+// w4_api.cu -- the C ABI of libw4 (include/w4.h): argument validation, dispatch, the decode-step
+// sequence and its CUDA graph, diagnostics, and the NF4 code-book construction.
+#include <atomic>
+#include <cerrno>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <vector>
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/w4.h"
+#include "w4_internal.h"
+
+namespace w4 {
+
+static std::atomic<long long> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static std::atomic<int> g_inject{0};
+int take_fault_injection() { return g_inject.exchange(0); }
+
+unsigned int read_clear_error_gemv();
+
+}  // namespace w4
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return W4_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return W4_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool pow2_in_range(int v) { return v >= 32 && v <= 256 && (v & (v - 1)) == 0; }
+
+// Shape rules shared by every call on a packed matrix.
+int check_shape(int N, int K, int bs) {
+  if (!pow2_in_range(bs)) return W4_ERR_BLOCKSIZE;
+  if (N < 1 || K < bs || K % bs != 0) return W4_ERR_SHAPE;
+  if (K > W4_MAX_K) return W4_ERR_UNSUPPORTED;
+  return W4_OK;
+}
+
+int check_gemv(int format, const uint8_t* packed, const void* scales, const float* codebook, const uint16_t* x,
+               const uint16_t* y, int M, int N, int K, int bs) {
+  if (format != W4_FMT_NF4 && format != W4_FMT_INT4) return W4_ERR_UNSUPPORTED;
+  if (!packed || !scales || !x || !y || (format == W4_FMT_NF4 && !codebook)) return W4_ERR_NULL;
+  int s = check_shape(N, K, bs);
+  if (s != W4_OK) return s;
+  if (M < 1) return W4_ERR_SHAPE;
+  if (M > W4_MAX_BATCH) return W4_ERR_UNSUPPORTED;
+  if (!aligned(packed, 16) || !aligned(scales, 16) || !aligned(x, 16) || !aligned(y, 2) ||
+      (codebook && !aligned(codebook, 4)))
+    return W4_ERR_ALIGN;
+  return W4_OK;
+}
+
+// Enqueue one validated GEMV.  Batches above one CUDA-core launch's budget are split into
+// launches over consecutive batch rows (each re-reads the weights).
+int enqueue_gemv(int format, const uint8_t* packed, const void* scales, const float* codebook, const uint16_t* x,
+                 uint16_t* y, int M, int N, int K, int bs, cudaStream_t stream) {
+  const __half* xh = reinterpret_cast<const __half*>(x);
+  __half* yh = reinterpret_cast<__half*>(y);
+  if (M >= 32) {
+    cudaError_t e = w4::launch_gemv_tc(format, packed, scales, codebook, xh, yh, M, N, K, bs, true, stream);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+  }
+  const int mb = w4::simt_max_batch(format, K, bs);
+  if (mb < 1) return W4_ERR_UNSUPPORTED;
+  for (int m0 = 0; m0 < M; m0 += mb) {
+    const int mm = (M - m0) < mb ? (M - m0) : mb;
+    cudaError_t e = w4::launch_gemv_simt(format, packed, scales, codebook, xh + (size_t)m0 * K,
+                                         yh + (size_t)m0 * N, mm, N, K, bs, true, stream);
+    if (e == cudaErrorNotSupported) return W4_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return W4_OK;
+}
+
+// Inverse of the standard normal CDF: Newton's method on Phi(x) - p with Phi(x) = erfc(-x/sqrt2)/2,
+// started at 0.  For p in [1/2, 1) the iterates increase monotonically to the root (Phi is concave
+// there), so the loop ends when a step no longer changes x.
+double inv_norm_cdf_upper(double p) {
+  const double kSqrt2 = 1.4142135623730951;
+  const double kInvSqrt2Pi = 0.3989422804014327;
+  double x = 0.0;
+  for (int i = 0; i < 200; ++i) {
+    const double f = 0.5 * std::erfc(-x / kSqrt2) - p;
+    const double d = kInvSqrt2Pi * std::exp(-0.5 * x * x);
+    const double nx = x - f / d;
+    if (nx == x) break;
+    x = nx;
+  }
+  return x;
+}
+
+}  // namespace
+
+struct w4_step {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  long long kernels = 0;
+};
+
+extern "C" {
+
+int w4_nf4_codebook(float out[16]) {
+  if (!out) return W4_ERR_NULL;
+  const double delta = 0.5 * ((1.0 - 1.0 / 32.0) + (1.0 - 1.0 / 30.0));
+  double v[16];
+  int n = 0;
+  for (int i = 0; i < 8; ++i) v[n++] = inv_norm_cdf_upper(delta + i * ((0.5 - delta) / 8.0));
+  for (int i = 0; i < 7; ++i) v[n++] = -inv_norm_cdf_upper(delta + i * ((0.5 - delta) / 7.0));
+  v[n++] = 0.0;
+  // ascending order (insertion sort of 16 values)
+  for (int i = 1; i < 16; ++i) {
+    double t = v[i];
+    int j = i - 1;
+    while (j >= 0 && v[j] > t) { v[j + 1] = v[j]; --j; }
+    v[j + 1] = t;
+  }
+  const double top = v[15];
+  for (int i = 0; i < 16; ++i) out[i] = static_cast<float>(v[i] / top);
+  return W4_OK;
+}
+
+int w4_quantize_nf4(const float* W, uint8_t* packed, float* absmax, const float* codebook, int N, int K,
+                    int blocksize, w4_stream_t stream) {
+  if (!W || !packed || !absmax || !codebook) return W4_ERR_NULL;
+  int s = check_shape(N, K, blocksize);
+  if (s != W4_OK) return s;
+  if (!aligned(W, 16) || !aligned(packed, 16) || !aligned(absmax, 16) || !aligned(codebook, 4)) return W4_ERR_ALIGN;
+  return cuda_status(w4::launch_quantize_nf4(W, packed, absmax, codebook, N, K, blocksize,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4_quantize_int4(const float* W, uint8_t* packed, uint16_t* scale, int N, int K, int group,
+                     w4_stream_t stream) {
+  if (!W || !packed || !scale) return W4_ERR_NULL;
+  int s = check_shape(N, K, group);
+  if (s != W4_OK) return s;
+  if (!aligned(W, 16) || !aligned(packed, 16) || !aligned(scale, 16)) return W4_ERR_ALIGN;
+  return cuda_status(w4::launch_quantize_int4(W, packed, reinterpret_cast<__half*>(scale), N, K, group,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4_dequantize_nf4(const uint8_t* packed, const float* absmax, const float* codebook, float* W_out, int N,
+                      int K, int blocksize, w4_stream_t stream) {
+  if (!packed || !absmax || !codebook || !W_out) return W4_ERR_NULL;
+  int s = check_shape(N, K, blocksize);
+  if (s != W4_OK) return s;
+  if (!aligned(W_out, 8) || !aligned(packed, 16) || !aligned(absmax, 16) || !aligned(codebook, 4)) return W4_ERR_ALIGN;
+  return cuda_status(w4::launch_dequantize_nf4(packed, absmax, codebook, W_out, N, K, blocksize,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4_dequantize_int4(const uint8_t* packed, const uint16_t* scale, float* W_out, int N, int K, int group,
+                       w4_stream_t stream) {
+  if (!packed || !scale || !W_out) return W4_ERR_NULL;
+  int s = check_shape(N, K, group);
+  if (s != W4_OK) return s;
+  if (!aligned(W_out, 8) || !aligned(packed, 16) || !aligned(scale, 16)) return W4_ERR_ALIGN;
+  return cuda_status(w4::launch_dequantize_int4(packed, reinterpret_cast<const __half*>(scale), W_out, N, K, group,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int w4_gemv_nf4(const uint8_t* packed, const float* absmax, const float* codebook, const uint16_t* x, uint16_t* y,
+                int M, int N, int K, int blocksize, w4_stream_t stream) {
+  int s = check_gemv(W4_FMT_NF4, packed, absmax, codebook, x, y, M, N, K, blocksize);
+  if (s != W4_OK) return s;
+  return enqueue_gemv(W4_FMT_NF4, packed, absmax, codebook, x, y, M, N, K, blocksize,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w4_gemv_int4(const uint8_t* packed, const uint16_t* scale, const uint16_t* x, uint16_t* y, int M, int N, int K,
+                 int group, w4_stream_t stream) {
+  int s = check_gemv(W4_FMT_INT4, packed, scale, nullptr, x, y, M, N, K, group);
+  if (s != W4_OK) return s;
+  return enqueue_gemv(W4_FMT_INT4, packed, scale, nullptr, x, y, M, N, K, group,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w4_gemv_sequence(const w4_gemv_desc* descs, int count, w4_stream_t stream) {
+  if (!descs) return W4_ERR_NULL;
+  if (count < 0) return W4_ERR_SHAPE;
+  for (int i = 0; i < count; ++i) {
+    const w4_gemv_desc& d = descs[i];
+    int s = check_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize);
+    if (s != W4_OK) return s;
+  }
+  for (int i = 0; i < count; ++i) {
+    const w4_gemv_desc& d = descs[i];
+    int s = enqueue_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize,
+                         reinterpret_cast<cudaStream_t>(stream));
+    if (s != W4_OK) return s;
+  }
+  return W4_OK;
+}
+
+int w4_step_create(const w4_gemv_desc* descs, int count, w4_step** out) {
+  if (!descs || !out) return W4_ERR_NULL;
+  *out = nullptr;
+  for (int i = 0; i < count; ++i) {
+    const w4_gemv_desc& d = descs[i];
+    int s = check_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize);
+    if (s != W4_OK) return s;
+  }
+  cudaStream_t cs = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_status(e);
+  w4_step* st = new w4_step();
+  const long long before = w4::g_launches.load();
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  int s = W4_OK;
+  if (e == cudaSuccess) {
+    for (int i = 0; i < count && s == W4_OK; ++i) {
+      const w4_gemv_desc& d = descs[i];
+      s = enqueue_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize, cs);
+    }
+    cudaError_t e2 = cudaStreamEndCapture(cs, &st->graph);
+    if (e == cudaSuccess) e = e2;
+  }
+  // launches recorded during capture are not executions; count them per replay instead
+  st->kernels = w4::g_launches.load() - before;
+  w4::g_launches.fetch_sub(st->kernels);
+  if (e == cudaSuccess && s == W4_OK) e = cudaGraphInstantiate(&st->exec, st->graph, 0);
+  cudaStreamDestroy(cs);
+  if (s != W4_OK || e != cudaSuccess) {
+    if (st->exec) cudaGraphExecDestroy(st->exec);
+    if (st->graph) cudaGraphDestroy(st->graph);
+    delete st;
+    return s != W4_OK ? s : cuda_status(e);
+  }
+  *out = st;
+  return W4_OK;
+}
+
+int w4_step_launch(w4_step* step, w4_stream_t stream) {
+  if (!step || !step->exec) return W4_ERR_NULL;
+  cudaError_t e = cudaGraphLaunch(step->exec, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) w4::g_launches.fetch_add(step->kernels);
+  return cuda_status(e);
+}
+
+int w4_step_destroy(w4_step* step) {
+  if (!step) return W4_ERR_NULL;
+  if (step->exec) cudaGraphExecDestroy(step->exec);
+  if (step->graph) cudaGraphDestroy(step->graph);
+  delete step;
+  return W4_OK;
+}
+
+const char* w4_status_str(int status) {
+  switch (status) {
+    case W4_OK: return "ok";
+    case W4_ERR_NULL: return "null pointer";
+    case W4_ERR_SHAPE: return "bad shape";
+    case W4_ERR_ALIGN: return "misaligned pointer";
+    case W4_ERR_BLOCKSIZE: return "block size must be a power of two in [32, 256]";
+    case W4_ERR_CUDA: return "CUDA runtime error";
+    case W4_ERR_TIMEOUT: return "device-side wait timed out";
+    case W4_ERR_UNSUPPORTED: return "unsupported by this build";
+    default: return "unknown status";
+  }
+}
+
+int w4_last_cuda_error(void) { return t_last_cuda_error; }
+
+int w4_device_check(w4_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  unsigned int v = w4::read_clear_error_gemv();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_status(e);
+  return v ? W4_ERR_TIMEOUT : W4_OK;
+}
+
+long long w4_launch_count(void) { return w4::g_launches.load(); }
+
+int w4_inject_timeout_once(void) {
+  w4::g_inject.store(1);
+  return W4_OK;
+}
+
+}  // extern "C"

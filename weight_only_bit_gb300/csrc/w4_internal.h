@@ -1,0 +1,42 @@
+// w4_internal.h -- host-side declarations shared by libw4's translation units (not installed).
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+// Increments the process-wide count of kernel launches issued by the library.
+void note_launch();
+
+// Test hook: returns 1 once (and clears the request) after w4_inject_timeout_once() was called.
+int take_fault_injection();
+
+cudaError_t launch_quantize_nf4(const float* W, uint8_t* packed, float* absmax, const float* codebook,
+                                int N, int K, int bs, cudaStream_t stream);
+cudaError_t launch_quantize_int4(const float* W, uint8_t* packed, __half* scale, int N, int K, int gs,
+                                 cudaStream_t stream);
+cudaError_t launch_dequantize_nf4(const uint8_t* packed, const float* absmax, const float* codebook,
+                                  float* out, int N, int K, int bs, cudaStream_t stream);
+cudaError_t launch_dequantize_int4(const uint8_t* packed, const __half* scale, float* out, int N, int K,
+                                   int gs, cudaStream_t stream);
+
+// One GEMV on CUDA cores (batch 1 ... 31).  Batches above the per-launch register budget are
+// split into several launches by the caller.  Returns cudaErrorNotSupported for shapes the
+// kernel does not serve.
+cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scales, const float* codebook,
+                             const __half* x, __half* y, int M, int N, int K, int bs, bool pdl,
+                             cudaStream_t stream);
+
+// One GEMV on the tensor cores (batch 32 ... 128).
+cudaError_t launch_gemv_tc(int format, const uint8_t* packed, const void* scales, const float* codebook,
+                           const __half* x, __half* y, int M, int N, int K, int bs, bool pdl,
+                           cudaStream_t stream);
+
+// Largest batch (8, 4, 2 or 1) one CUDA-core launch serves for this format, K and block size
+// (0 if none: the shape is unsupported).
+int simt_max_batch(int format, int K, int bs);
+
+int device_sm_count();
+
+}  // namespace w4

@@ -1,0 +1,132 @@
+"""Decode-step driver: the 197 projection GEMVs of one Qwen2.5-1.5B-shaped decode step, run back
+to back on one stream and replayed as one CUDA graph ("Do Quantization and Sparsity make LLM
+Inference Faster ?", section "What we did": eight shapes, 197 GEMVs per token; "My Triton Kernel
+Ties bitsandbytes", section "What's next": CUDA graphs around the decode step).
+
+Weights are synthetic (synth.weights, N(0, 0.02)) and quantised on the GPU by libw4.  All
+activations live in one contiguous device arena and all outputs in another, so a host round trip
+is one copy each way.  Each GEMV reads x only after every earlier GEMV of the step has completed
+(stream order + programmatic dependent launch), as in a real decode step.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import synth
+from . import _lib
+import weight_only_bit_gb300 as w4
+
+
+def _align8(n: int) -> int:
+    return (n + 7) // 8 * 8
+
+
+class DecodeStep:
+    def __init__(self, fmt: str = "nf4", batch: int = 1, device: str = "cuda:0", blocksize: int | None = None,
+                 outlier_frac: float = 0.0, layers: int = synth.N_LAYERS, lm_head: bool = True):
+        import torch
+        self.torch = torch
+        self.fmt = fmt
+        self.format = _lib.W4_FMT_NF4 if fmt == "nf4" else _lib.W4_FMT_INT4
+        self.bs = blocksize or (64 if fmt == "nf4" else 128)
+        self.M = batch
+        self.dev = torch.device(device)
+        self.outlier_frac = outlier_frac
+        self.gemvs = [g for g in synth.decode_step_gemvs()
+                      if (g[1] != "lm_head" and g[0] < layers) or (g[1] == "lm_head" and lm_head)]
+        # x slots: (layer, slot) -> offset in the x arena
+        self.x_off = {}
+        off = 0
+        for layer, proj, n, k in self.gemvs:
+            key = (layer, synth.X_SLOT[proj])
+            if key not in self.x_off:
+                self.x_off[key] = (off, k)
+                off += _align8(batch * k)
+        self.x_elems = off
+        self.y_off = []
+        off = 0
+        for layer, proj, n, k in self.gemvs:
+            self.y_off.append(off)
+            off += _align8(batch * n)
+        self.y_elems = off
+        self.code = None
+        self.packed, self.scales = [], []
+        self.step = None
+
+    # ------------------------------------------------------------------ setup
+    def build(self, seed_offset: int = 0):
+        torch = self.torch
+        if self.format == _lib.W4_FMT_NF4:
+            st, c = w4.w4_nf4_codebook()
+            w4.check(st, "codebook")
+            self.code = torch.tensor(c, dtype=torch.float32, device=self.dev)
+        self.x = torch.empty(self.x_elems, dtype=torch.float16, device=self.dev)
+        self.y = torch.zeros(self.y_elems, dtype=torch.float16, device=self.dev)
+        xs = np.zeros(self.x_elems, dtype=np.float16)
+        for (layer, slot), (o, k) in self.x_off.items():
+            xs[o:o + self.M * k] = synth.activations(synth.x_seed(layer, slot, self.M), self.M, k).ravel()
+        self.x.copy_(torch.from_numpy(xs))
+        self.x_host = xs
+        for layer, proj, n, k in self.gemvs:
+            w = synth.weights(synth.weight_seed(layer, proj) + seed_offset, n, k, outlier_frac=self.outlier_frac)
+            W = torch.from_numpy(w).to(self.dev)
+            packed = torch.empty((n, k // 2), dtype=torch.uint8, device=self.dev)
+            if self.format == _lib.W4_FMT_NF4:
+                sc = torch.empty((n, k // self.bs), dtype=torch.float32, device=self.dev)
+                w4.check(w4.w4_quantize_nf4(W, packed, sc, self.code, n, k, self.bs), f"quantize {proj}")
+            else:
+                sc = torch.empty((n, k // self.bs), dtype=torch.float16, device=self.dev)
+                w4.check(w4.w4_quantize_int4(W, packed, sc, n, k, self.bs), f"quantize {proj}")
+            self.packed.append(packed)
+            self.scales.append(sc)
+            del W
+        torch.cuda.synchronize(self.dev)
+        return self
+
+    def descriptors(self):
+        d = []
+        for i, (layer, proj, n, k) in enumerate(self.gemvs):
+            xo, _ = self.x_off[(layer, synth.X_SLOT[proj])]
+            d.append(dict(format=self.format, packed=self.packed[i], scales=self.scales[i], codebook=self.code,
+                          x=self.x.data_ptr() + 2 * xo, y=self.y.data_ptr() + 2 * self.y_off[i],
+                          M=self.M, N=n, K=k, blocksize=self.bs))
+        return d
+
+    def capture(self):
+        st, h = w4.w4_step_create(self.descriptors())
+        w4.check(st, "step create")
+        self.step = h
+        return self
+
+    def launch(self, stream=None):
+        return w4.w4_step_launch(self.step, stream)
+
+    def enqueue_eager(self, stream=None):
+        return w4.w4_gemv_sequence(self.descriptors(), stream)
+
+    def close(self):
+        if self.step is not None:
+            w4.w4_step_destroy(self.step)
+            self.step = None
+
+    # ------------------------------------------------------------------ accounting
+    def scale_bytes(self, n: int, k: int) -> int:
+        return n * (k // self.bs) * (4 if self.format == _lib.W4_FMT_NF4 else 2)
+
+    def gemv_bytes(self, i: int) -> int:
+        """Algorithmic bytes of GEMV i: packed weights + scales + x + y (each touched once)."""
+        _, _, n, k = self.gemvs[i]
+        return n * k // 2 + self.scale_bytes(n, k) + 2 * self.M * k + 2 * self.M * n
+
+    def bytes_per_step(self) -> int:
+        return sum(self.gemv_bytes(i) for i in range(len(self.gemvs)))
+
+    def y_of(self, i: int):
+        _, _, n, _ = self.gemvs[i]
+        o = self.y_off[i]
+        return self.y[o:o + self.M * n].view(self.M, n)
+
+    def x_of(self, i: int):
+        layer, proj, n, k = self.gemvs[i]
+        o, _ = self.x_off[(layer, synth.X_SLOT[proj])]
+        return self.x_host[o:o + self.M * k].reshape(self.M, k)

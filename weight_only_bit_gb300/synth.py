@@ -19,6 +19,9 @@ model's weights and hidden states, with the model's shapes.
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 BASE_SEED = 20261202
@@ -73,23 +76,72 @@ def decode_step_gemvs():
     yield N_LAYERS, "lm_head", n, k
 
 
+ROW_BLOCK = 1024   # rows per independently seeded generator block
+
+
+def _fill_block(seed: int, b: int, k: int, rows: int, sigma: float) -> np.ndarray:
+    out = np.empty((rows, k), dtype=np.float32)
+    np.random.Generator(np.random.PCG64([seed, b])).standard_normal(out=out, dtype=np.float32)
+    out *= np.float32(sigma)
+    return out
+
+
+def _outliers(seed: int, n: int, k: int, frac: float, sigmas: float, sigma: float):
+    count = int(round(frac * n * k))
+    rng = np.random.Generator(np.random.PCG64([seed, 1 << 40]))
+    pos = rng.choice(n * k, size=count, replace=False)
+    sign = np.where(rng.random(count) < 0.5, -1.0, 1.0)
+    return pos, (sign * sigmas * sigma).astype(np.float32)
+
+
 def weights(seed: int, n: int, k: int, sigma: float = 0.02,
             outlier_frac: float = 0.0, outlier_sigmas: float = 10.0) -> np.ndarray:
     """FP32 weight matrix [n, k] with entries N(0, sigma).
 
-    With outlier_frac > 0, exactly round(outlier_frac * n * k) distinct positions,
-    drawn without replacement, are replaced by +-outlier_sigmas * sigma with a
-    random sign (the 0.1 % outliers at 10 sigma of the outlier sweep).
+    Rows come in blocks of ROW_BLOCK, block b drawn by PCG64 seeded with (seed, b), so the matrix
+    is the same whatever the number of threads, and any rows can be regenerated alone.
+    With outlier_frac > 0, exactly round(outlier_frac * n * k) distinct positions, drawn without
+    replacement, are replaced by +-outlier_sigmas * sigma with a random sign (the 0.1 % outliers
+    at 10 sigma of the outlier sweep).
     """
-    rng = np.random.default_rng(seed)
-    w = rng.standard_normal((n, k), dtype=np.float32)
-    w *= np.float32(sigma)
+    nb = (n + ROW_BLOCK - 1) // ROW_BLOCK
+    w = np.empty((n, k), dtype=np.float32)
+
+    def fill(b):
+        r0 = b * ROW_BLOCK
+        r1 = min(n, r0 + ROW_BLOCK)
+        w[r0:r1] = _fill_block(seed, b, k, r1 - r0, sigma)
+
+    if nb > 1:
+        with ThreadPoolExecutor(max_workers=min(nb, os.cpu_count() or 4)) as ex:
+            list(ex.map(fill, range(nb)))
+    else:
+        fill(0)
     if outlier_frac > 0.0:
-        count = int(round(outlier_frac * n * k))
-        pos = rng.choice(n * k, size=count, replace=False)
-        sign = np.where(rng.random(count) < 0.5, -1.0, 1.0)
-        w.reshape(-1)[pos] = (sign * outlier_sigmas * sigma).astype(np.float32)
+        pos, val = _outliers(seed, n, k, outlier_frac, outlier_sigmas, sigma)
+        w.reshape(-1)[pos] = val
     return w
+
+
+def weights_rows(seed: int, n: int, k: int, rows, sigma: float = 0.02,
+                 outlier_frac: float = 0.0, outlier_sigmas: float = 10.0) -> np.ndarray:
+    """Rows `rows` of weights(seed, n, k, ...), generating only the blocks that hold them."""
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.empty((len(rows), k), dtype=np.float32)
+    blocks = {}
+    for i, r in enumerate(rows):
+        b = int(r) // ROW_BLOCK
+        if b not in blocks:
+            r0 = b * ROW_BLOCK
+            blocks[b] = _fill_block(seed, b, k, min(n, r0 + ROW_BLOCK) - r0, sigma)
+        out[i] = blocks[b][int(r) - b * ROW_BLOCK]
+    if outlier_frac > 0.0:
+        pos, val = _outliers(seed, n, k, outlier_frac, outlier_sigmas, sigma)
+        pr, pc = pos // k, pos % k
+        for i, r in enumerate(rows):
+            sel = pr == r
+            out[i, pc[sel]] = val[sel]
+    return out
 
 
 def activations(seed: int, m: int, k: int) -> np.ndarray:
