@@ -131,9 +131,11 @@ int w4_gemv_int4(const uint8_t* packed, const uint16_t* scale,
                  w4_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
- * Decode step: the projections of one decode step launched back to back ("Do Quantization and
- * Sparsity make LLM Inference Faster ?", section "What we did": 197 GEMVs per token), each
- * GEMV reading x only after every earlier GEMV of the sequence has completed.
+ * Decode step: the projections of one decode step ("Do Quantization and Sparsity make LLM
+ * Inference Faster ?", section "What we did": 197 GEMVs per token).  Descriptors carry a level:
+ * levels start at 0 and never decrease along the array; the GEMVs of one level are independent
+ * of each other (e.g. q, k and v, which read the same activation), and a level reads x only after
+ * every GEMV of the earlier levels is complete.
  */
 typedef struct {
   int format;               /* w4_format                                               */
@@ -143,17 +145,28 @@ typedef struct {
   const uint16_t* x;        /* [M][K] fp16                                              */
   uint16_t* y;              /* [M][N] fp16                                              */
   int M, N, K, blocksize;
+  int level;                /* dependency level, see above                              */
 } w4_gemv_desc;
 
-/* Validates every descriptor, then enqueues the GEMVs in order on `stream`. */
+/* Validates every descriptor, then enqueues one GEMV launch per descriptor, in order, on `stream`
+ * (each launch reads x after the previous one completed). */
 int w4_gemv_sequence(const w4_gemv_desc* descs, int count, w4_stream_t stream);
 
-/* A decode step captured once into a CUDA graph.  w4_step_create validates, captures the
- * sequence on a private stream and instantiates the graph (host-side objects only; no device
- * buffers are allocated); w4_step_launch replays it on `stream`.  The descriptors' pointers are
- * baked into the graph: the buffers must outlive the step. */
+/* Device workspace (bytes) that w4_step_create needs for `count` descriptors: one 32-bit counter
+ * per level plus one. */
+int64_t w4_step_workspace_bytes(int count);
+
+/* A decode step captured once into a CUDA graph.  When every descriptor has the same format,
+ * batch M <= 8 and (NF4) the same code book, the whole step is ONE persistent launch: every CTA
+ * streams the weights of all levels ahead through its shared-memory ring and each level starts
+ * reading x when the counters in `workspace` show the previous level complete.  Otherwise the
+ * step is one launch per GEMV.  `workspace`: device memory of w4_step_workspace_bytes(count) bytes,
+ * 16-byte aligned, owned by the caller, used only by this step; w4_step_create zeroes it (and
+ * synchronises), every launch leaves it zero again.  Launches of one step must not overlap on
+ * the GPU (stream order guarantees that).  The descriptors' pointers are baked into the graph:
+ * the buffers must outlive the step.  No device memory is allocated. */
 typedef struct w4_step w4_step;
-int w4_step_create(const w4_gemv_desc* descs, int count, w4_step** out);
+int w4_step_create(const w4_gemv_desc* descs, int count, void* workspace, w4_step** out);
 int w4_step_launch(w4_step* step, w4_stream_t stream);
 int w4_step_destroy(w4_step* step);
 

@@ -75,12 +75,21 @@ def test_quantize_and_dequantize_validation(libw4):
 
 def test_sequence_and_step_validation(libw4):
     d = (_lib.GemvDesc * 2)()
-    d[0] = _lib.GemvDesc(_lib.W4_FMT_NF4, A, A, A, A, A, 1, 256, 1536, 64)
-    d[1] = _lib.GemvDesc(_lib.W4_FMT_INT4, A, A, 0, A, A, 1, 256, 1536, 100)   # bad group
-    assert libw4.w4_gemv_sequence(d, 2, None) == _lib.W4_ERR_BLOCKSIZE           # nothing enqueued
+    d[0] = _lib.GemvDesc(_lib.W4_FMT_NF4, A, A, A, A, A, 1, 256, 1536, 64, 0)
+    d[1] = _lib.GemvDesc(_lib.W4_FMT_INT4, A, A, 0, A, A, 1, 256, 1536, 100, 1)   # bad group
+    assert libw4.w4_gemv_sequence(d, 2, None) == _lib.W4_ERR_BLOCKSIZE            # nothing enqueued
     assert libw4.w4_gemv_sequence(None, 2, None) == _lib.W4_ERR_NULL
     h = ctypes.c_void_p()
-    assert libw4.w4_step_create(d, 2, ctypes.byref(h)) == _lib.W4_ERR_BLOCKSIZE and h.value is None
+    assert libw4.w4_step_create(d, 2, A, ctypes.byref(h)) == _lib.W4_ERR_BLOCKSIZE and h.value is None
+    d[1] = _lib.GemvDesc(_lib.W4_FMT_NF4, A, A, A, A, A, 1, 256, 1536, 64, 2)      # level jumps by 2
+    assert libw4.w4_gemv_sequence(d, 2, None) == _lib.W4_ERR_SHAPE
+    d[1].level = 0
+    d[0].level = 1                                                                # first level must be 0
+    assert libw4.w4_gemv_sequence(d, 2, None) == _lib.W4_ERR_SHAPE
+    d[0].level = 0
+    assert libw4.w4_step_create(d, 2, None, ctypes.byref(h)) == _lib.W4_ERR_NULL    # persistent needs workspace
+    assert libw4.w4_step_create(d, 2, A + 4, ctypes.byref(h)) == _lib.W4_ERR_ALIGN
+    assert libw4.w4_step_workspace_bytes(197) >= 4 * 198 and libw4.w4_step_workspace_bytes(0) == 0
     assert libw4.w4_step_launch(None, None) == _lib.W4_ERR_NULL
     assert libw4.w4_step_destroy(None) == _lib.W4_ERR_NULL
     d[0].format = 7

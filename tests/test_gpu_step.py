@@ -38,15 +38,18 @@ def _check_step(step, rows_per_gemv=8, seed=0):
         assert np.all(rel <= 1e-3), (layer, proj, rel)
 
 
-def test_full_nf4_step_graph(dev):
+@pytest.mark.parametrize("levels", ["grouped", "strict"])
+def test_full_nf4_step_graph(dev, levels):
     from weight_only_bit_gb300.step import DecodeStep
-    step = DecodeStep("nf4", batch=1, device=str(dev)).build().capture()
+    step = DecodeStep("nf4", batch=1, device=str(dev), levels=levels).build().capture()
     assert len(step.gemvs) == 197
+    assert step.levels[-1] == (112 if levels == "grouped" else 196)
     stream = torch.cuda.Stream(dev)
     l0 = w4.w4_launch_count()
     w4.check(step.launch(stream))
     torch.cuda.synchronize()
-    assert w4.w4_launch_count() - l0 == 197
+    assert w4.w4_launch_count() - l0 == 1                  # the whole step is one persistent launch
+    assert torch.all(step.workspace == 0)                  # counters left at zero for the next launch
     assert w4.w4_device_check(stream) == 0
     g = step.y.clone()
     _check_step(step)
@@ -55,15 +58,18 @@ def test_full_nf4_step_graph(dev):
     w4.check(step.enqueue_eager(stream))
     torch.cuda.synchronize()
     assert torch.equal(step.y.view(torch.int16), g.view(torch.int16))
-    # replaying twice changes nothing
-    w4.check(step.launch(stream))
-    w4.check(step.launch(stream))
+    # replaying back to back (programmatic launch overlap between replays) changes nothing
+    step.y.fill_(float("nan"))
+    for _ in range(5):
+        w4.check(step.launch(stream))
     torch.cuda.synchronize()
+    assert w4.w4_device_check(stream) == 0
     assert torch.equal(step.y.view(torch.int16), g.view(torch.int16))
+    assert torch.all(step.workspace == 0)
     step.close()
 
 
-@pytest.mark.parametrize("fmt,batch", [("int4", 1), ("nf4", 8), ("int4", 8), ("nf4", 32)])
+@pytest.mark.parametrize("fmt,batch", [("int4", 1), ("nf4", 3), ("nf4", 8), ("int4", 8), ("nf4", 32)])
 def test_reduced_steps(dev, fmt, batch):
     from weight_only_bit_gb300.step import DecodeStep
     step = DecodeStep(fmt, batch=batch, device=str(dev), layers=2, lm_head=False,
@@ -73,4 +79,26 @@ def test_reduced_steps(dev, fmt, batch):
     torch.cuda.synchronize()
     assert w4.w4_device_check(stream) == 0
     _check_step(step, rows_per_gemv=16, seed=1)
+    step.close()
+
+
+def test_step_timeout_path_recovers(dev):
+    """The injected producer failure inside a multi-level persistent step: every bounded wait ends,
+    the host reads W4_ERR_TIMEOUT, the counters are left at zero and the next replay is right."""
+    from weight_only_bit_gb300.step import DecodeStep
+    step = DecodeStep("nf4", batch=1, device=str(dev), layers=1, lm_head=False)
+    step.build()
+    stream = torch.cuda.Stream(dev)
+    w4.w4_inject_timeout_once()
+    step.capture()                       # the hook applies to the captured launch
+    w4.check(step.launch(stream))
+    torch.cuda.synchronize()
+    assert w4.w4_device_check(stream) == w4._lib.W4_ERR_TIMEOUT
+    assert torch.all(step.workspace == 0)
+    step.close()
+    step.capture()
+    w4.check(step.launch(stream))
+    torch.cuda.synchronize()
+    assert w4.w4_device_check(stream) == 0
+    _check_step(step, rows_per_gemv=16, seed=2)
     step.close()

@@ -15,7 +15,8 @@ from ._lib import (GemvDesc, W4Error, lib, SYMBOLS, W4_OK, W4_ERR_NULL, W4_ERR_S
 
 __all__ = [
     "w4_nf4_codebook", "w4_quantize_nf4", "w4_quantize_int4", "w4_dequantize_nf4", "w4_dequantize_int4",
-    "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_create", "w4_step_launch",
+    "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_workspace_bytes", "w4_step_create",
+    "w4_step_launch",
     "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check", "w4_launch_count",
     "w4_inject_timeout_once",
     "check", "W4Error", "GemvDesc", "W4_FMT_NF4", "W4_FMT_INT4", "W4_MAX_BATCH", "W4_MAX_K",
@@ -83,21 +84,26 @@ def _descs(descs):
     arr = (GemvDesc * len(descs))()
     for i, d in enumerate(descs):
         arr[i] = GemvDesc(d["format"], _ptr(d["packed"]), _ptr(d["scales"]), _ptr(d.get("codebook")),
-                          _ptr(d["x"]), _ptr(d["y"]), d["M"], d["N"], d["K"], d["blocksize"])
+                          _ptr(d["x"]), _ptr(d["y"]), d["M"], d["N"], d["K"], d["blocksize"], d.get("level", i))
     return arr
 
 
 def w4_gemv_sequence(descs, stream=None):
-    """descs: sequence of dicts with keys format, packed, scales, codebook, x, y, M, N, K, blocksize."""
+    """descs: sequence of dicts with keys format, packed, scales, codebook, x, y, M, N, K, blocksize and
+    optionally level (default: the descriptor's index, i.e. every GEMV waits for the one before)."""
     arr = _descs(descs)
     return lib().w4_gemv_sequence(arr, len(descs), _stream(stream))
 
 
-def w4_step_create(descs):
-    """Returns (status, handle)."""
+def w4_step_workspace_bytes(count: int) -> int:
+    return lib().w4_step_workspace_bytes(count)
+
+
+def w4_step_create(descs, workspace):
+    """Returns (status, handle).  workspace: device buffer of w4_step_workspace_bytes(len(descs))."""
     arr = _descs(descs)
     h = ctypes.c_void_p()
-    st = lib().w4_step_create(arr, len(descs), ctypes.byref(h))
+    st = lib().w4_step_create(arr, len(descs), _ptr(workspace), ctypes.byref(h))
     return st, h.value
 
 

@@ -27,7 +27,7 @@ W4_MAX_K = 10240
 # Every symbol include/w4.h declares.
 SYMBOLS = (
     "w4_nf4_codebook", "w4_quantize_nf4", "w4_quantize_int4", "w4_dequantize_nf4",
-    "w4_dequantize_int4", "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_create",
+    "w4_dequantize_int4", "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_workspace_bytes", "w4_step_create",
     "w4_step_launch", "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check",
     "w4_launch_count", "w4_inject_timeout_once",
 )
@@ -61,6 +61,7 @@ class GemvDesc(ctypes.Structure):
         ("N", ctypes.c_int),
         ("K", ctypes.c_int),
         ("blocksize", ctypes.c_int),
+        ("level", ctypes.c_int),
     ]
 
 
@@ -78,7 +79,8 @@ def _declare(L):
         "w4_gemv_nf4": (I, [P, P, P, P, P, I, I, I, I, P]),
         "w4_gemv_int4": (I, [P, P, P, P, I, I, I, I, P]),
         "w4_gemv_sequence": (I, [ctypes.POINTER(GemvDesc), I, P]),
-        "w4_step_create": (I, [ctypes.POINTER(GemvDesc), I, ctypes.POINTER(P)]),
+        "w4_step_workspace_bytes": (ctypes.c_int64, [I]),
+        "w4_step_create": (I, [ctypes.POINTER(GemvDesc), I, P, ctypes.POINTER(P)]),
         "w4_step_launch": (I, [P, P]),
         "w4_step_destroy": (I, [P]),
         "w4_status_str": (ctypes.c_char_p, [I]),

@@ -186,42 +186,88 @@ int w4_gemv_int4(const uint8_t* packed, const uint16_t* scale, const uint16_t* x
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
-int w4_gemv_sequence(const w4_gemv_desc* descs, int count, w4_stream_t stream) {
+static int check_descs(const w4_gemv_desc* descs, int count) {
   if (!descs) return W4_ERR_NULL;
-  if (count < 0) return W4_ERR_SHAPE;
+  if (count < 1) return W4_ERR_SHAPE;
+  int prev_level = 0;
   for (int i = 0; i < count; ++i) {
     const w4_gemv_desc& d = descs[i];
     int s = check_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize);
     if (s != W4_OK) return s;
+    const int want_lo = (i == 0) ? 0 : prev_level;
+    if (d.level < want_lo || d.level > (i == 0 ? 0 : prev_level + 1)) return W4_ERR_SHAPE;
+    prev_level = d.level;
   }
+  return W4_OK;
+}
+
+int w4_gemv_sequence(const w4_gemv_desc* descs, int count, w4_stream_t stream) {
+  int s = check_descs(descs, count);
+  if (s != W4_OK) return s;
   for (int i = 0; i < count; ++i) {
     const w4_gemv_desc& d = descs[i];
-    int s = enqueue_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize,
-                         reinterpret_cast<cudaStream_t>(stream));
+    s = enqueue_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize,
+                     reinterpret_cast<cudaStream_t>(stream));
     if (s != W4_OK) return s;
   }
   return W4_OK;
 }
 
-int w4_step_create(const w4_gemv_desc* descs, int count, w4_step** out) {
-  if (!descs || !out) return W4_ERR_NULL;
-  *out = nullptr;
+int64_t w4_step_workspace_bytes(int count) {
+  if (count < 1) return 0;
+  return ((int64_t)(count + 1) * 4 + 255) / 256 * 256;
+}
+
+// True when the step can run as one persistent CUDA-core launch.
+static bool step_is_persistent(const w4_gemv_desc* descs, int count) {
+  if (count > w4::kStepMaxGemvs) return false;
   for (int i = 0; i < count; ++i) {
     const w4_gemv_desc& d = descs[i];
-    int s = check_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize);
-    if (s != W4_OK) return s;
+    if (d.format != descs[0].format || d.M != descs[0].M || d.M > 8) return false;
+    if (d.format == W4_FMT_NF4 && d.codebook != descs[0].codebook) return false;
+    if (w4::simt_max_batch(d.format, d.K, d.blocksize) < d.M) return false;
   }
+  return true;
+}
+
+int w4_step_create(const w4_gemv_desc* descs, int count, void* workspace, w4_step** out) {
+  if (!out) return W4_ERR_NULL;
+  *out = nullptr;
+  int s = check_descs(descs, count);
+  if (s != W4_OK) return s;
+  const bool persistent = step_is_persistent(descs, count);
+  if (persistent && !workspace) return W4_ERR_NULL;
+  if (workspace && !aligned(workspace, 16)) return W4_ERR_ALIGN;
   cudaStream_t cs = nullptr;
   cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e != cudaSuccess) return cuda_status(e);
+  if (persistent) {
+    e = cudaMemsetAsync(workspace, 0, (size_t)w4_step_workspace_bytes(count), cs);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+    if (e != cudaSuccess) {
+      cudaStreamDestroy(cs);
+      return cuda_status(e);
+    }
+  }
   w4_step* st = new w4_step();
   const long long before = w4::g_launches.load();
   e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
-  int s = W4_OK;
   if (e == cudaSuccess) {
-    for (int i = 0; i < count && s == W4_OK; ++i) {
-      const w4_gemv_desc& d = descs[i];
-      s = enqueue_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize, cs);
+    if (persistent) {
+      std::vector<w4::StepJob> jobs((size_t)count);
+      for (int i = 0; i < count; ++i) {
+        const w4_gemv_desc& d = descs[i];
+        jobs[i] = w4::StepJob{d.packed, d.scales, reinterpret_cast<const __half*>(d.x), reinterpret_cast<__half*>(d.y),
+                              d.N, d.K, d.blocksize, d.level};
+      }
+      cudaError_t e3 = w4::launch_step_simt(descs[0].format, jobs.data(), count, descs[0].M, descs[0].codebook,
+                                            reinterpret_cast<unsigned*>(workspace), true, cs);
+      if (e3 != cudaSuccess) s = (e3 == cudaErrorNotSupported) ? W4_ERR_UNSUPPORTED : cuda_status(e3);
+    } else {
+      for (int i = 0; i < count && s == W4_OK; ++i) {
+        const w4_gemv_desc& d = descs[i];
+        s = enqueue_gemv(d.format, d.packed, d.scales, d.codebook, d.x, d.y, d.M, d.N, d.K, d.blocksize, cs);
+      }
     }
     cudaError_t e2 = cudaStreamEndCapture(cs, &st->graph);
     if (e == cudaSuccess) e = e2;

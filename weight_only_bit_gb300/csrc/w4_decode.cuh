@@ -1,0 +1,211 @@
+// w4_decode.cuh -- on-chip decoding of packed 4-bit weights against x held in registers.
+//
+// One "chunk" is 16 packed bytes = 32 consecutive weights of one row.  A consumer thread owns one
+// chunk position of x and multiplies it with that chunk of many rows.
+//
+//   NF4 ("LLM Quantization on RTX 4060", sections "Standard Expectation from Quantization" and
+//   "Kernel Implementation"): a 256-entry table indexed by a whole packed byte returns both code
+//   values (FP16) as one half2, element 2j in the low half; one copy of the table per lane, entry b
+//   of lane l at word b * 32 + l, so any pattern of bytes across a warp is conflict-free.  Products
+//   FP16 x FP16 are exact in FP32 (mixed-precision FMA), sums are FP32, and the block's FP32 absmax
+//   multiplies the chunk's partial sum.
+//
+//   INT4 ("My Triton Kernel Ties bitsandbytes", section "The kernels"): w_hat = (q - 8) * s.  x is
+//   converted once to 16-bit fixed point with one exponent per chunk, X = x * 2^(15 - E) where
+//   max |x| < 2^E (exact for every |x| >= 2^(E-5)), and split into a signed high byte and an
+//   unsigned low byte; dp4a multiplies four nibbles (isolated as bytes) with four digits, so
+//   sum (q - 8) x = 2^(E-15) * (256 sum q Xh + sum q Xl - 8 sum X), scaled by s.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "w4_common.cuh"
+
+namespace w4 {
+
+constexpr int kLutBytes = 256 * 32 * 4;   // NF4 byte-pair table, one copy per lane
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// x read through L2 only: it may have been written by another SM earlier in the same launch.
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// acc += lo(c) * lo(x) + hi(c) * hi(x); products exact (FP16 x FP16 fits FP32), FP32 sums.
+__device__ __forceinline__ void mixed_dot2(float& acc, uint32_t c2, uint32_t x2) {
+  asm("{\n .reg .f16 c0, c1, x0, x1;\n"
+      " mov.b32 {c0, c1}, %1;\n mov.b32 {x0, x1}, %2;\n"
+      " fma.rn.f32.f16 %0, c0, x0, %0;\n fma.rn.f32.f16 %0, c1, x1, %0;\n}"
+      : "+f"(acc) : "r"(c2), "r"(x2));
+}
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Builds the NF4 byte-pair table: entry b = half2(fp16(code[b >> 4]), fp16(code[b & 15])),
+// replicated for every lane.  Called by `nthreads` threads numbered t.
+__device__ __forceinline__ void build_nf4_lut(uint32_t* lut, const float* __restrict__ codebook, int t, int nthreads) {
+  for (int i = t; i < 256 * 32; i += nthreads) {
+    const int b = i >> 5;
+    const __half lo = __float2half_rn(__ldg(codebook + (b >> 4)));
+    const __half hi = __float2half_rn(__ldg(codebook + (b & 15)));
+    lut[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+  }
+}
+
+// x of one chunk, for MB batch rows.  NF4: 16 half2 pairs per row.  INT4: 16 digit words per row
+// (for packed word i: high and low bytes of X at elements 8i+1,3,5,7 -- the low nibbles -- then at
+// 8i+0,2,4,6 -- the high nibbles), plus the chunk factor 2^(E-15) and 8 * sum X.
+template <int FMT, int MB>
+struct XSlice {
+  uint32_t v[MB][16];
+  float f[MB];
+  int s8[MB];
+};
+
+// x: FROM_SMEM ? this CTA's shared-memory copy of x : x in global memory (read through L2).
+template <int FMT, int MB, bool FROM_SMEM>
+__device__ __forceinline__ void load_x_slice(XSlice<FMT, MB>& xs, const __half* __restrict__ x, int M, int K,
+                                             int chunk) {
+#pragma unroll
+  for (int m = 0; m < MB; ++m) {
+    uint32_t h[16];
+    if (m < M) {
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(x + (size_t)m * K + (size_t)chunk * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 q = FROM_SMEM ? *reinterpret_cast<const uint4*>(src + 16 * i) : ld_cg_v4(src + 16 * i);
+        h[4 * i + 0] = q.x; h[4 * i + 1] = q.y; h[4 * i + 2] = q.z; h[4 * i + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) h[i] = 0u;
+    }
+    if (FMT == 0) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xs.v[m][i] = h[i];
+      xs.f[m] = 1.0f;
+      xs.s8[m] = 0;
+    } else {
+      float xf[32];
+      float mx = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        __half2 hh = *reinterpret_cast<__half2*>(&h[i]);
+        float2 f2 = __half22float2(hh);
+        xf[2 * i] = f2.x;
+        xf[2 * i + 1] = f2.y;
+        mx = fmaxf(mx, fmaxf(fabsf(f2.x), fabsf(f2.y)));
+      }
+      int E = 0;
+      (void)frexpf(mx, &E);                 // mx < 2^E (mx == 0 gives E = 0)
+      const float up = ldexpf(1.0f, 15 - E);
+      int X[32];
+      int sx = 0;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        X[e] = __float2int_rn(xf[e] * up);  // |X| <= 32752
+        sx += X[e];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t ho = 0, lo = 0, he = 0, le = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int eo = 8 * i + 2 * b + 1, ee = 8 * i + 2 * b;
+          ho |= (uint32_t)((X[eo] >> 8) & 0xff) << (8 * b);
+          lo |= (uint32_t)(X[eo] & 0xff) << (8 * b);
+          he |= (uint32_t)((X[ee] >> 8) & 0xff) << (8 * b);
+          le |= (uint32_t)(X[ee] & 0xff) << (8 * b);
+        }
+        xs.v[m][4 * i + 0] = ho;
+        xs.v[m][4 * i + 1] = lo;
+        xs.v[m][4 * i + 2] = he;
+        xs.v[m][4 * i + 3] = le;
+      }
+      xs.f[m] = ldexpf(1.0f, E - 15);
+      xs.s8[m] = 8 * sx;
+    }
+  }
+}
+
+// One chunk of one row: part[m] = sum over the chunk's 32 weights of w_hat * x[m].
+// wv: the chunk's 16 packed bytes; scale_addr: shared-memory address of the row's scale for the
+// chunk (FP32 absmax for NF4, FP16 s for INT4); lut_lane: this lane's table base (NF4).
+template <int FMT, int MB>
+__device__ __forceinline__ void chunk_dot(float (&part)[MB], const uint4 wv, uint32_t scale_addr, uint32_t lut_lane,
+                                          const XSlice<FMT, MB>& xs) {
+  const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+  if (FMT == 0) {
+    const float a = __uint_as_float(lds32(scale_addr));
+    constexpr int NA = MB >= 4 ? 1 : 4 / MB;   // independent accumulators per batch row
+    float acc[MB][NA];
+#pragma unroll
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+      for (int q = 0; q < NA; ++q) acc[m][q] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        uint32_t byte;
+        asm("prmt.b32 %0, %1, 0, %2;" : "=r"(byte) : "r"(w4[i]), "r"(0x4440 + b));
+        const uint32_t c2 = lds32(lut_lane + byte * 128u);
+#pragma unroll
+        for (int m = 0; m < MB; ++m) mixed_dot2(acc[m][(4 * i + b) % NA], c2, xs.v[m][4 * i + b]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+      float s = 0.0f;
+#pragma unroll
+      for (int q = 0; q < NA; ++q) s += acc[m][q];
+      part[m] = s * a;
+    }
+  } else {
+    const float s = __half2float(__ushort_as_half((unsigned short)lds_u16(scale_addr)));
+    int ah[MB], al[MB];
+#pragma unroll
+    for (int m = 0; m < MB; ++m) { ah[m] = 0; al[m] = 0; }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = w4[i] & 0x0f0f0f0fu;
+      const uint32_t hi = (w4[i] >> 4) & 0x0f0f0f0fu;
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        ah[m] = dp4a_us(lo, xs.v[m][4 * i + 0], ah[m]);
+        al[m] = dp4a_uu(lo, xs.v[m][4 * i + 1], al[m]);
+        ah[m] = dp4a_us(hi, xs.v[m][4 * i + 2], ah[m]);
+        al[m] = dp4a_uu(hi, xs.v[m][4 * i + 3], al[m]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+      const int tot = ah[m] * 256 + al[m] - xs.s8[m];
+      part[m] = (float)tot * (s * xs.f[m]);
+    }
+  }
+}
+
+}  // namespace w4

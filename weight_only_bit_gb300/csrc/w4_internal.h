@@ -21,9 +21,8 @@ cudaError_t launch_dequantize_nf4(const uint8_t* packed, const float* absmax, co
 cudaError_t launch_dequantize_int4(const uint8_t* packed, const __half* scale, float* out, int N, int K,
                                    int gs, cudaStream_t stream);
 
-// One GEMV on CUDA cores (batch 1 ... 31).  Batches above the per-launch register budget are
-// split into several launches by the caller.  Returns cudaErrorNotSupported for shapes the
-// kernel does not serve.
+// One GEMV on CUDA cores (batches 1 ... 8 per launch; the caller splits larger batches).  Returns
+// cudaErrorNotSupported for shapes the kernel does not serve.
 cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scales, const float* codebook,
                              const __half* x, __half* y, int M, int N, int K, int bs, bool pdl,
                              cudaStream_t stream);
@@ -38,5 +37,20 @@ cudaError_t launch_gemv_tc(int format, const uint8_t* packed, const void* scales
 int simt_max_batch(int format, int K, int bs);
 
 int device_sm_count();
+
+// A whole decode step in one persistent CUDA-core launch.  GEMVs are grouped into levels (0, 1, ...
+// non-decreasing along the array); a level reads its x only after every GEMV of the previous level
+// is complete.  counters: caller-owned device memory of (number of levels + 1) words, zero before
+// the first launch; the kernel leaves it zero again.
+constexpr int kStepMaxGemvs = 256;
+struct StepJob {
+  const uint8_t* packed;
+  const void* scales;
+  const __half* x;
+  __half* y;
+  int N, K, bs, level;
+};
+cudaError_t launch_step_simt(int format, const StepJob* jobs, int n, int M, const float* codebook, unsigned* counters,
+                             bool pdl, cudaStream_t stream);
 
 }  // namespace w4

@@ -1,0 +1,561 @@
+// w4_persist.cu -- fused 4-bit dequant-GEMV on CUDA cores (batches 1 ... 31), one persistent,
+// warp-specialised kernel for a single GEMV or for every GEMV of a decode step (sm_103a).
+//
+// Computes y[m][n] = sum_k w_hat[n][k] * x[m][k] with w_hat decoded on chip, FP32 accumulation and
+// an FP16 result; no dequantised matrix ever reaches DRAM ("LLM Quantization on RTX 4060: Where
+// 4-bit Decode Falls Behind FP16", sections "Fused Kernel: Moving Dequantization On-Chip" and
+// "Kernel Implementation").
+//
+// Work: each GEMV is cut into tiles of whole rows (rows are contiguous in memory, so a tile is one
+// span).  GEMVs are grouped into levels; a level's GEMVs are independent of each other (the
+// projections of one decode layer that read the same activation: q, k, v / o / gate, up / down).
+// A level's x is read only after every tile of the previous level is complete, which models the
+// decode step's data dependencies ("Do Quantization and Sparsity make LLM Inference Faster ?",
+// section "What we did": the 197 GEMVs of one step).  Level 0 waits for the previous kernel in the
+// stream (programmatic dependent launch); later levels wait on tile counters in global memory.
+// Tile t of a level goes to CTA t mod gridDim.x; the grid is sized to be co-resident.
+//
+// Roles in a CTA:
+//   * producer warp: streams each tile's packed bytes and scales into a 3-stage shared-memory ring
+//     with 1-D bulk async copies (TMA unit), mbarrier completion, an L2 evict-first hint; it runs
+//     ahead across level boundaries (weights never depend on other GEMVs);
+//   * consumer warps: thread (rho, chunk) owns one 32-weight column chunk, keeps that slice of x in
+//     registers for the whole level, and produces one partial sum per (row, chunk);
+//   * reducer warp: sums each row's partials in a fixed order (lanes over chunks, then a warp
+//     shuffle: the reduction idiom of "Do Quantization and Sparsity make LLM Inference Faster ?",
+//     "Optional: what does the custom kernel actually do?"), writes y, and publishes tile
+//     completion; partial buffers are double-buffered, so consumers never wait for a reduction.
+// Every wait is bounded in wall-clock time; a lost wait is recorded in the device error word and
+// the kernel runs to its end without further waiting.
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "w4_common.cuh"
+#include "w4_decode.cuh"
+#include "w4_internal.h"
+
+namespace w4 {
+
+constexpr int kStages = 3;
+constexpr int kMaxConsumers = 320;      // consumer threads: one per chunk of a row x rows per sweep
+constexpr int kTargetConsumers = 288;
+constexpr int kStageTarget = 12288;     // packed bytes per stage (about)
+constexpr int kXCap = 18432;            // largest x (M x K x 2 bytes) staged in shared memory
+
+struct PGemv {
+  const uint8_t* packed;
+  const void* scales;
+  const __half* x;
+  __half* y;
+  int N, K, bs, rpt;       // rpt: rows per tile
+  int tile0, ntiles, srb;  // global tile range; scale bytes per row
+  int cpr;                 // chunks per row (K / 32)
+};
+
+struct PLevel {
+  int gemv0, ngemv, tile0, ntiles;
+};
+
+template <int MAXL, int MAXG>
+struct PParams {
+  const float* codebook;
+  unsigned int* counters;  // [nlevels + 1] when nlevels > 1, else null
+  int nlevels, ngemvs, M, inject_timeout;
+  int stage_w, stage_s, red_floats, n_consumer_warps;
+  int x_bytes;             // shared-memory x buffer (0: every thread reads its x slice from L2)
+  PLevel lv[MAXL];
+  PGemv gm[MAXG];
+};
+
+struct PLayout {
+  int lut, x, w, s, red, bar, total;
+};
+
+__host__ __device__ inline PLayout playout(int fmt, int stage_w, int stage_s, int red_floats, int x_bytes) {
+  PLayout L;
+  int off = 0;
+  L.lut = 0;
+  if (fmt == 0) off += kLutBytes;
+  L.x = off;
+  off += x_bytes;
+  L.w = off;
+  off += kStages * stage_w;
+  L.s = off;
+  off += kStages * stage_s;
+  L.red = off;
+  off += 2 * red_floats * 4;
+  off = (off + 15) & ~15;
+  L.bar = off;
+  off += (2 * kStages + 4) * 8;
+  L.total = off;
+  return L;
+}
+
+__device__ __forceinline__ int first_owned(int tile0) {
+  const int G = (int)gridDim.x;
+  const int b = (int)blockIdx.x;
+  return tile0 + (((b - tile0) % G) + G) % G;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait until *p >= target (other CTAs' releases).  Records `site` on timeout.
+__device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned target, uint32_t site) {
+  if (ld_acquire_u32(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(128);
+    if (ld_acquire_u32(p) >= target) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+  }
+  atomicCAS(&g_error_word, 0u, site);
+  return false;
+}
+
+template <int FMT, int MB, int MAXL, int MAXG>
+__global__ void __launch_bounds__(kMaxConsumers + 64, 1) w4_persistent_kernel(const __grid_constant__ PParams<MAXL, MAXG> p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const PLayout Lo = playout(FMT, p.stage_w, p.stage_s, p.red_floats, p.x_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lo.bar);
+  uint64_t* empty = full + kStages;
+  uint64_t* rfull = empty + kStages;
+  uint64_t* rfree = rfull + 2;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ncw = p.n_consumer_warps;
+  const int n_cons = ncw * 32;
+  const int G = (int)gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], ncw);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&rfull[i], ncw);
+      mbar_init(&rfree[i], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp == ncw) {
+    // ================================================================ producer warp
+    if (p.inject_timeout) return;   // test hook: nothing issued, nothing in flight
+    const uint64_t pol = policy_evict_first();
+    int j = 0;
+    bool ok = true;
+    for (int L = 0; L < p.nlevels; ++L) {
+      const PLevel lv = p.lv[L];
+      int g = lv.gemv0;
+      for (int t = first_owned(lv.tile0); t < lv.tile0 + lv.ntiles; t += G, ++j) {
+        while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
+        const PGemv gm = p.gm[g];
+        const int st = j % kStages;
+        const int round = j / kStages;
+        // Prefetch of the first kStages tiles may overlap the previous kernel in the stream; the
+        // bounded waits start only once that kernel is complete.
+        if (round == 1 && st == 0) pdl_wait();
+        if (lane == 0 && round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1, 0x201);
+        const int r0 = (t - gm.tile0) * gm.rpt;
+        const int nrows = min(gm.rpt, gm.N - r0);
+        const uint32_t wbytes = (uint32_t)nrows * (uint32_t)(gm.K / 2);
+        const uint32_t sbytes = (uint32_t)nrows * (uint32_t)gm.srb;
+        const uint32_t sbulk = sbytes & ~15u;
+        uint8_t* dst_w = smem + Lo.w + st * p.stage_w;
+        uint8_t* dst_s = smem + Lo.s + st * p.stage_s;
+        const uint8_t* src_s = reinterpret_cast<const uint8_t*>(gm.scales) + (size_t)r0 * gm.srb;
+        if (lane == 0) {
+          if (ok) {
+            for (uint32_t b = sbulk; b < sbytes; ++b) dst_s[b] = src_s[b];   // sub-16-byte tail
+            mbar_arrive_expect_tx(&full[st], wbytes + sbulk);
+            bulk_g2s(dst_w, gm.packed + (size_t)r0 * (gm.K / 2), wbytes, &full[st], pol);
+            if (sbulk) bulk_g2s(dst_s, src_s, sbulk, &full[st], pol);
+          } else {
+            mbar_arrive(&full[st]);
+          }
+        }
+        __syncwarp();
+      }
+    }
+    // never leave while bulk copies into this CTA's shared memory may be in flight
+    if (lane == 0) {
+      for (int k = (j > kStages ? j - kStages : 0); k < j; ++k) mbar_wait(&full[k % kStages], (k / kStages) & 1, 0x202);
+    }
+    return;
+  }
+
+  float* red_base = reinterpret_cast<float*>(smem + Lo.red);
+
+  if (warp == ncw + 1) {
+    // ================================================================ reducer warp
+    pdl_wait();   // counters are touched only after the previous kernel in the stream completed
+    int j = 0;
+    bool ok = true;
+    for (int L = 0; L < p.nlevels; ++L) {
+      const PLevel lv = p.lv[L];
+      int g = lv.gemv0;
+      const int t_end = lv.tile0 + lv.ntiles;
+      for (int t = first_owned(lv.tile0); t < t_end; t += G, ++j) {
+        while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
+        const PGemv gm = p.gm[g];
+        const int b = j & 1;
+        if (lane == 0 && ok) ok = mbar_wait(&rfull[b], (j >> 1) & 1, 0x203);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        const int r0 = (t - gm.tile0) * gm.rpt;
+        const int nrows = min(gm.rpt, gm.N - r0);
+        const float* red = red_base + b * p.red_floats;
+        // one lane per output (row x batch row); each row sums its partials in one fixed order that
+        // depends only on K (eight interleaved accumulators, then a fixed tree), so a row gets the
+        // same bits whatever the tiling
+        const int outs = nrows * MB;
+        const int stride = gm.cpr + 1;             // odd row stride: conflict-free column reads
+        for (int o = lane; o < outs; o += 32) {
+          const int m = o / nrows;
+          const int lr = o - m * nrows;
+          const float* rr = red + (m * gm.rpt + lr) * stride;
+          float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          int c = 0;
+          for (; c + 7 < gm.cpr; c += 8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] += rr[c + i];
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (c + i < gm.cpr) a[i] += rr[c + i];
+          }
+          const float v = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+          if (m < p.M) gm.y[(size_t)m * gm.N + r0 + lr] = __float2half_rn(v);
+        }
+        const bool publish = p.counters && t + G >= t_end;   // this CTA's last tile of level L
+        if (publish) __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&rfree[b]);
+          if (publish) {
+            __threadfence();
+            atomicAdd(&p.counters[L], 1u);
+          }
+        }
+      }
+    }
+    // end of the launch: the last CTA to finish resets the counters for the next launch
+    asm volatile("bar.sync 2, %0;" ::"r"(n_cons + 32) : "memory");
+    if (p.counters && lane == 0) {
+      __threadfence();
+      const unsigned done = atomicAdd(&p.counters[p.nlevels], 1u);
+      if (done == (unsigned)G - 1) {
+        for (int L = 0; L <= p.nlevels; ++L) atomicExch(&p.counters[L], 0u);
+      }
+    }
+    return;
+  }
+
+  // ================================================================== consumer warps
+  const int tid = threadIdx.x;
+  const uint32_t lut_lane = smem_u32(smem + Lo.lut) + (uint32_t)lane * 4u;
+  if (FMT == 0) build_nf4_lut(reinterpret_cast<uint32_t*>(smem + Lo.lut), p.codebook, tid, n_cons);
+  asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
+
+  XSlice<FMT, MB> xs;
+  const __half* x_loaded = nullptr;
+  int k_loaded = -1;
+  int rho = 0, chunk = 0, rps = 1;
+  bool active = false;
+  int j = 0;
+  bool ok = true;
+  bool pdl_done = false;
+  for (int L = 0; L < p.nlevels; ++L) {
+    const PLevel lv = p.lv[L];
+    const int t_first = first_owned(lv.tile0);
+    if (t_first >= lv.tile0 + lv.ntiles) continue;           // no tile of this level here
+    // ---- wait until this level's inputs exist
+    if (!pdl_done) {
+      pdl_wait();
+      pdl_done = true;
+    }
+    if (L > 0 && p.counters) {
+      // every CTA that owns a tile of level L-1 adds one when it has finished them all
+      const unsigned owners = (unsigned)min(G, p.lv[L - 1].ntiles);
+      if (tid == 0 && ok) ok = wait_counter(&p.counters[L - 1], owners, 0x204);
+      asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
+    }
+    int g = lv.gemv0;
+    for (int t = t_first; t < lv.tile0 + lv.ntiles; t += G, ++j) {
+      while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
+      const PGemv gm = p.gm[g];
+      if (gm.x != x_loaded || gm.K != k_loaded) {
+        const int cpr = gm.cpr;
+        rps = cpr >= kTargetConsumers ? 1 : kTargetConsumers / cpr;
+        rho = tid / cpr;
+        chunk = tid - rho * cpr;
+        active = rho < rps;
+        const int xb = p.M * gm.K * 2;
+        if (xb <= p.x_bytes) {
+          // one coalesced copy of x per CTA (16-byte pieces through L2), then each thread takes
+          // its slice from shared memory: every SM reads x once instead of once per thread
+          __half* xsm = reinterpret_cast<__half*>(smem + Lo.x);
+          asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");    // previous x no longer read
+          for (int i = tid; i < xb / 16; i += n_cons) {
+            reinterpret_cast<uint4*>(xsm)[i] = ld_cg_v4(reinterpret_cast<const uint8_t*>(gm.x) + 16 * i);
+          }
+          asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
+          if (active) load_x_slice<FMT, MB, true>(xs, xsm, p.M, gm.K, chunk);
+        } else if (active) {
+          load_x_slice<FMT, MB, false>(xs, gm.x, p.M, gm.K, chunk);
+        }
+        x_loaded = gm.x;
+        k_loaded = gm.K;
+      }
+      const int st = j % kStages;
+      const int b = j & 1;
+      // lane 0 of each warp polls, the warp follows
+      if (lane == 0) {
+        if (ok) ok = mbar_wait(&full[st], (j / kStages) & 1, 0x205);
+        if (j >= 2 && ok) ok = mbar_wait(&rfree[b], ((j >> 1) - 1) & 1, 0x206);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      const int r0 = (t - gm.tile0) * gm.rpt;
+      const int nrows = min(gm.rpt, gm.N - r0);
+      const uint32_t sw = smem_u32(smem + Lo.w + st * p.stage_w);
+      const uint32_t ss = smem_u32(smem + Lo.s + st * p.stage_s);
+      float* red = red_base + b * p.red_floats;
+      if (active && ok) {
+        const int es = FMT == 0 ? 4 : 2;
+        const uint32_t soff = (uint32_t)(((chunk * 32) / gm.bs) * es);
+        for (int lr = rho; lr < nrows; lr += rps) {
+          const uint4 wv = lds128(sw + (uint32_t)(lr * (gm.K / 2) + chunk * 16));
+          float part[MB];
+          chunk_dot<FMT, MB>(part, wv, ss + (uint32_t)(lr * gm.srb) + soff, lut_lane, xs);
+#pragma unroll
+          for (int m = 0; m < MB; ++m) red[(m * gm.rpt + lr) * (gm.cpr + 1) + chunk] = part[m];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&empty[st]);
+        mbar_arrive(&rfull[b]);
+      }
+    }
+  }
+  asm volatile("bar.sync 2, %0;" ::"r"(n_cons + 32) : "memory");
+}
+
+// ====================================================================== host side
+static int g_sm_count = 0;
+
+int device_sm_count() {
+  if (g_sm_count == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sm_count <= 0) g_sm_count = 1;
+  }
+  return g_sm_count;
+}
+
+static int gcd_int(int a, int b) {
+  while (b) { int t = a % b; a = b; b = t; }
+  return a;
+}
+
+static int batch_block(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
+
+// Per-GEMV geometry that does not depend on the tiling.
+struct GeomG {
+  int cpr, srb, align_rows, rpt_max, ncw, rps;
+};
+
+static bool geom(int fmt, int K, int bs, GeomG& o) {
+  o.cpr = K / 32;
+  if (o.cpr < 1 || o.cpr > kMaxConsumers) return false;
+  const int rps = o.cpr >= kTargetConsumers ? 1 : kTargetConsumers / o.cpr;
+  o.ncw = (rps * o.cpr + 31) / 32;
+  o.srb = (K / bs) * (fmt == 0 ? 4 : 2);
+  o.align_rows = 16 / gcd_int(o.srb, 16);       // keeps every tile's scale span 16-byte aligned
+  // about kStageTarget packed bytes, rounded to a whole number of consumer sweeps
+  const int r = kStageTarget / (K / 2);
+  int sweeps = (r + rps / 2) / rps;
+  if (sweeps < 1) sweeps = 1;
+  o.rps = rps;
+  o.rpt_max = ((sweeps * rps + o.align_rows - 1) / o.align_rows) * o.align_rows;
+  return true;
+}
+
+struct Job {
+  const uint8_t* packed;
+  const void* scales;
+  const __half* x;
+  __half* y;
+  int N, K, bs, level;
+};
+
+// Layout of a set of GEMVs at batch block MB (independent of tiling, which never exceeds rpt_max).
+static bool plan_layout(int fmt, int MB, int M, const Job* jobs, int n, int& stage_w, int& stage_s,
+                        int& red_floats, int& ncw, int& x_bytes, PLayout& L) {
+  stage_w = 16; stage_s = 16; red_floats = 1; ncw = 1; x_bytes = 0;
+  for (int i = 0; i < n; ++i) {
+    GeomG gg;
+    if (!geom(fmt, jobs[i].K, jobs[i].bs, gg)) return false;
+    stage_w = max(stage_w, gg.rpt_max * (jobs[i].K / 2));
+    stage_s = max(stage_s, ((gg.rpt_max * gg.srb) + 15) & ~15);
+    red_floats = max(red_floats, MB * gg.rpt_max * (gg.cpr + 1));
+    ncw = max(ncw, gg.ncw);
+    const int xb = M * jobs[i].K * 2;
+    if (xb <= kXCap) x_bytes = max(x_bytes, xb);
+  }
+  L = playout(fmt, stage_w, stage_s, red_floats, x_bytes);
+  return L.total <= 227 * 1024;
+}
+
+int simt_max_batch(int format, int K, int bs) {
+  Job jb{nullptr, nullptr, nullptr, nullptr, 1, K, bs, 0};
+  for (int m : {8, 4, 2, 1}) {
+    int sw, ss, rf, ncw, xb;
+    PLayout L;
+    if (plan_layout(format, m, m, &jb, 1, sw, ss, rf, ncw, xb, L)) return m;
+  }
+  return 0;
+}
+
+template <int FMT, int MB, int MAXL, int MAXG>
+static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float* codebook, unsigned* counters,
+                                     bool pdl, cudaStream_t stream) {
+  using P = PParams<MAXL, MAXG>;
+  auto kern = w4_persistent_kernel<FMT, MB, MAXL, MAXG>;
+  P* pp = new P();   // large parameter block: build on the heap
+  P& p = *pp;
+  int nlev = 0;
+  for (int i = 0; i < n; ++i) nlev = max(nlev, jobs[i].level + 1);
+  if (n > MAXG || nlev > MAXL) { delete pp; return cudaErrorNotSupported; }
+  int stage_w, stage_s, red_floats, ncw, x_bytes;
+  PLayout L;
+  if (!plan_layout(FMT, MB, M, jobs, n, stage_w, stage_s, red_floats, ncw, x_bytes, L)) {
+    delete pp;
+    return cudaErrorNotSupported;
+  }
+  static bool attr_done = false;   // one flag per instance
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) { delete pp; return e; }
+    attr_done = true;
+  }
+  const int threads = ncw * 32 + 64;
+  static int occ_threads = -1, occ_smem = -1, occ_val = 1;
+  if (occ_threads != threads || occ_smem != L.total) {
+    int v = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, (size_t)L.total);
+    if (e != cudaSuccess) { delete pp; return e; }
+    occ_threads = threads; occ_smem = L.total; occ_val = v < 1 ? 1 : (v > 2 ? 2 : v);
+  }
+  const int gmax = device_sm_count() * occ_val;
+  p.codebook = codebook;
+  p.counters = nlev > 1 ? counters : nullptr;
+  if (nlev > 1 && !counters) { delete pp; return cudaErrorInvalidValue; }
+  p.nlevels = nlev;
+  p.ngemvs = n;
+  p.M = M;
+  p.inject_timeout = take_fault_injection();
+  p.stage_w = stage_w; p.stage_s = stage_s; p.red_floats = red_floats; p.n_consumer_warps = ncw;
+  p.x_bytes = x_bytes;
+  // tiling, level by level: balanced tiles per CTA, rows per tile within each GEMV's stage budget
+  int tile = 0, max_level_tiles = 0;
+  for (int Lv = 0, i = 0; Lv < nlev; ++Lv) {
+    const int first = i;
+    long long rows = 0;
+    int rmin = 1 << 30;
+    while (i < n && jobs[i].level == Lv) {
+      GeomG gg;
+      geom(FMT, jobs[i].K, jobs[i].bs, gg);
+      rows += jobs[i].N;
+      rmin = min(rmin, gg.rpt_max);
+      ++i;
+    }
+    p.lv[Lv].gemv0 = first;
+    p.lv[Lv].ngemv = i - first;
+    p.lv[Lv].tile0 = tile;
+    const long long tpc = (rows + (long long)gmax * rmin - 1) / ((long long)gmax * rmin);
+    for (int q = first; q < i; ++q) {
+      GeomG gg;
+      geom(FMT, jobs[q].K, jobs[q].bs, gg);
+      int rpt = (int)((rows + (long long)gmax * tpc - 1) / ((long long)gmax * tpc));
+      if (rpt > gg.rps) rpt = ((rpt + gg.rps - 1) / gg.rps) * gg.rps;   // whole sweeps when it can
+      rpt = ((rpt + gg.align_rows - 1) / gg.align_rows) * gg.align_rows;
+      rpt = min(rpt, gg.rpt_max);
+      PGemv& g = p.gm[q];
+      g.packed = jobs[q].packed; g.scales = jobs[q].scales; g.x = jobs[q].x; g.y = jobs[q].y;
+      g.N = jobs[q].N; g.K = jobs[q].K; g.bs = jobs[q].bs; g.rpt = rpt;
+      g.tile0 = tile; g.ntiles = (g.N + rpt - 1) / rpt; g.srb = gg.srb; g.cpr = gg.cpr;
+      tile += g.ntiles;
+    }
+    p.lv[Lv].ntiles = tile - p.lv[Lv].tile0;
+    max_level_tiles = max(max_level_tiles, p.lv[Lv].ntiles);
+  }
+  const int grid = nlev > 1 ? gmax : min(gmax, max_level_tiles);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  note_launch();
+  delete pp;
+  return e;
+}
+
+template <int MAXL, int MAXG>
+static cudaError_t dispatch(int fmt, int MB, const Job* jobs, int n, int M, const float* codebook, unsigned* counters,
+                            bool pdl, cudaStream_t s) {
+  if (fmt == 0) {
+    switch (MB) {
+      case 1: return launch_persistent<0, 1, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
+      case 2: return launch_persistent<0, 2, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
+      case 4: return launch_persistent<0, 4, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
+      default: return launch_persistent<0, 8, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
+    }
+  }
+  switch (MB) {
+    case 1: return launch_persistent<1, 1, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
+    case 2: return launch_persistent<1, 2, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
+    case 4: return launch_persistent<1, 4, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
+    default: return launch_persistent<1, 8, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
+  }
+}
+
+cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scales, const float* codebook,
+                             const __half* x, __half* y, int M, int N, int K, int bs, bool pdl,
+                             cudaStream_t stream) {
+  if (M < 1 || M > 8) return cudaErrorNotSupported;
+  Job jb{packed, scales, x, y, N, K, bs, 0};
+  return dispatch<1, 1>(format, batch_block(M), &jb, 1, M, codebook, nullptr, pdl, stream);
+}
+
+cudaError_t launch_step_simt(int format, const StepJob* jobs, int n, int M, const float* codebook, unsigned* counters,
+                             bool pdl, cudaStream_t stream) {
+  if (M < 1 || M > 8 || n < 1 || n > kStepMaxGemvs) return cudaErrorNotSupported;
+  Job js[kStepMaxGemvs];
+  for (int i = 0; i < n; ++i) {
+    js[i] = Job{jobs[i].packed, jobs[i].scales, jobs[i].x, jobs[i].y, jobs[i].N, jobs[i].K, jobs[i].bs, jobs[i].level};
+  }
+  return dispatch<kStepMaxGemvs, kStepMaxGemvs>(format, batch_block(M), js, n, M, codebook, counters, pdl, stream);
+}
+
+unsigned int read_clear_error_gemv() {
+  unsigned int v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v));
+  cudaMemcpyToSymbol(g_error_word, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace w4

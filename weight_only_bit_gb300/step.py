@@ -23,7 +23,11 @@ def _align8(n: int) -> int:
 
 class DecodeStep:
     def __init__(self, fmt: str = "nf4", batch: int = 1, device: str = "cuda:0", blocksize: int | None = None,
-                 outlier_frac: float = 0.0, layers: int = synth.N_LAYERS, lm_head: bool = True):
+                 outlier_frac: float = 0.0, layers: int = synth.N_LAYERS, lm_head: bool = True,
+                 levels: str = "grouped"):
+        """levels="grouped": GEMVs reading the same activation form one level (q,k,v / o / gate,up /
+        down / lm_head: 113 levels for the full step); levels="strict": every GEMV waits for the one
+        before it (197 levels)."""
         import torch
         self.torch = torch
         self.fmt = fmt
@@ -49,6 +53,14 @@ class DecodeStep:
             self.y_off.append(off)
             off += _align8(batch * n)
         self.y_elems = off
+        self.levels = []
+        lev, prev = -1, None
+        for i, (layer, proj, n, k) in enumerate(self.gemvs):
+            key = (layer, synth.X_SLOT[proj])
+            if levels == "strict" or key != prev:
+                lev += 1
+            prev = key
+            self.levels.append(lev)
         self.code = None
         self.packed, self.scales = [], []
         self.step = None
@@ -89,11 +101,14 @@ class DecodeStep:
             xo, _ = self.x_off[(layer, synth.X_SLOT[proj])]
             d.append(dict(format=self.format, packed=self.packed[i], scales=self.scales[i], codebook=self.code,
                           x=self.x.data_ptr() + 2 * xo, y=self.y.data_ptr() + 2 * self.y_off[i],
-                          M=self.M, N=n, K=k, blocksize=self.bs))
+                          M=self.M, N=n, K=k, blocksize=self.bs, level=self.levels[i]))
         return d
 
     def capture(self):
-        st, h = w4.w4_step_create(self.descriptors())
+        torch = self.torch
+        nbytes = w4.w4_step_workspace_bytes(len(self.gemvs))
+        self.workspace = torch.zeros(nbytes // 4, dtype=torch.int32, device=self.dev)
+        st, h = w4.w4_step_create(self.descriptors(), self.workspace)
         w4.check(st, "step create")
         self.step = h
         return self
@@ -102,6 +117,7 @@ class DecodeStep:
         return w4.w4_step_launch(self.step, stream)
 
     def enqueue_eager(self, stream=None):
+        """One launch per GEMV, back to back (the same results, without the persistent step)."""
         return w4.w4_gemv_sequence(self.descriptors(), stream)
 
     def close(self):
@@ -130,3 +146,47 @@ class DecodeStep:
         layer, proj, n, k = self.gemvs[i]
         o, _ = self.x_off[(layer, synth.X_SLOT[proj])]
         return self.x_host[o:o + self.M * k].reshape(self.M, k)
+
+
+def _main():
+    """Run a decode step on cuda:0 and print its device time (also the workload the ncu
+    summaries under profiles/ were captured on)."""
+    import argparse
+    import torch
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--fmt", default="nf4", choices=["nf4", "int4"])
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=synth.N_LAYERS)
+    ap.add_argument("--no-lm-head", action="store_true")
+    ap.add_argument("--levels", default="grouped", choices=["grouped", "strict"])
+    ap.add_argument("--launch-per-gemv", action="store_true", help="one launch per GEMV instead of one per step")
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    a = ap.parse_args()
+    from weight_only_bit_gb300 import build as _b
+    _b.build()
+    st = DecodeStep(a.fmt, a.batch, "cuda:0", layers=a.layers, lm_head=not a.no_lm_head, levels=a.levels).build()
+    stream = torch.cuda.Stream()
+    if a.launch_per_gemv:
+        run = lambda: w4.check(st.enqueue_eager(stream))
+    else:
+        st.capture()
+        run = lambda: w4.check(st.launch(stream))
+    for _ in range(a.warmup):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(a.steps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    w4.check(w4.w4_device_check(stream))
+    ms = e0.elapsed_time(e1) / a.steps
+    print(f"{a.fmt} batch {a.batch}, {len(st.gemvs)} GEMVs, {st.levels[-1] + 1} levels: {ms * 1e3:.1f} us/step, "
+          f"{st.bytes_per_step() / (ms * 1e-3) / 1e9:.1f} GB/s")
+    st.close()
+
+
+if __name__ == "__main__":
+    _main()
