@@ -60,7 +60,8 @@ typedef enum {
   W4_ERR_BLOCKSIZE = -4,   /* block / group size is not a power of two in [32, 256]          */
   W4_ERR_CUDA = -5,        /* a CUDA runtime call failed; see w4_last_cuda_error()          */
   W4_ERR_TIMEOUT = -6,     /* a bounded device-side wait ran out (reported by w4_device_check) */
-  W4_ERR_UNSUPPORTED = -7  /* valid arguments outside what this build implements           */
+  W4_ERR_UNSUPPORTED = -7, /* valid arguments outside what this build implements           */
+  W4_ERR_LIMIT = -8        /* beyond the fixed size of w4_gemv_levels_noalloc's counter array */
 } w4_status;
 
 typedef enum { W4_FMT_NF4 = 0, W4_FMT_INT4 = 1 } w4_format;
@@ -169,6 +170,29 @@ typedef struct w4_step w4_step;
 int w4_step_create(const w4_gemv_desc* descs, int count, void* workspace, w4_step** out);
 int w4_step_launch(w4_step* step, w4_stream_t stream);
 int w4_step_destroy(w4_step* step);
+
+/* ---------------------------------------------------------------------------------------
+ * w4_gemv_levels_noalloc -- runs the descriptors as ONE persistent launch on `stream`, like
+ * w4_step_create + w4_step_launch, without any device memory from the caller beyond its inputs
+ * and outputs.  The pages have no counterpart of this entry point.  It is for callers that cannot
+ * allocate device memory: code running inside a device-memory allocator or pool callback (a
+ * cudaMalloc there re-enters the allocator), processes whose device memory a framework's caching
+ * allocator has reserved up front (a cudaMalloc there fails or fragments the pool), serving loops
+ * that forbid allocation after warm-up (cudaMalloc can synchronise the device and stall every
+ * stream), and plugin interfaces that hand the callee only its input and output buffers.
+ * The level counters that w4_step_create keeps in a caller workspace live here in a fixed array
+ * inside libw4 (W4_NOALLOC_MAX_LEVELS + 1 32-bit words, held on every GPU that loads the library
+ * until the process exits).  Limits: at most W4_NOALLOC_MAX_LEVELS levels and W4_NOALLOC_MAX_GEMVS
+ * descriptors, else W4_ERR_LIMIT.  Same conditions as the single-launch step (one format,
+ * M <= 8, one code book), else W4_ERR_UNSUPPORTED.  Each call first clears the counters it uses
+ * (an asynchronous memset on `stream`), then launches; it never calls cudaMalloc, cudaFree or
+ * any allocating routine.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture.  Every call uses the same array, so calls that overlap on the GPU (other streams,
+ * other host threads) race and give wrong results: serialise them. */
+#define W4_NOALLOC_MAX_LEVELS 256
+#define W4_NOALLOC_MAX_GEMVS 256
+int w4_gemv_levels_noalloc(const w4_gemv_desc* descs, int count, w4_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Diagnostics. */

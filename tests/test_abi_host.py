@@ -97,7 +97,7 @@ def test_sequence_and_step_validation(libw4):
 
 
 def test_status_strings(libw4):
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         assert libw4.w4_status_str(code)
     assert w4.w4_status_str(_lib.W4_ERR_ALIGN) != w4.w4_status_str(_lib.W4_ERR_SHAPE)
     with pytest.raises(w4.W4Error):

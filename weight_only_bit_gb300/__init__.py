@@ -18,7 +18,7 @@ __all__ = [
     "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_workspace_bytes", "w4_step_create",
     "w4_step_launch",
     "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check", "w4_launch_count",
-    "w4_inject_timeout_once",
+    "w4_inject_timeout_once", "w4_gemv_levels_noalloc",
     "check", "W4Error", "GemvDesc", "W4_FMT_NF4", "W4_FMT_INT4", "W4_MAX_BATCH", "W4_MAX_K",
 ]
 
@@ -133,3 +133,10 @@ def w4_launch_count() -> int:
 
 def w4_inject_timeout_once() -> int:
     return lib().w4_inject_timeout_once()
+
+
+def w4_gemv_levels_noalloc(descs, stream=None) -> int:
+    """One persistent launch of the descriptors with the level counters inside libw4, for callers
+    that cannot allocate device memory; see include/w4.h for its limits and its one-time set-up."""
+    arr = _descs(descs)
+    return lib().w4_gemv_levels_noalloc(arr, len(descs), _stream(stream))

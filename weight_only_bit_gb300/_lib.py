@@ -19,6 +19,9 @@ W4_ERR_BLOCKSIZE = -4
 W4_ERR_CUDA = -5
 W4_ERR_TIMEOUT = -6
 W4_ERR_UNSUPPORTED = -7
+W4_ERR_LIMIT = -8
+W4_NOALLOC_MAX_LEVELS = 256
+W4_NOALLOC_MAX_GEMVS = 256
 W4_FMT_NF4 = 0
 W4_FMT_INT4 = 1
 W4_MAX_BATCH = 128
@@ -29,7 +32,7 @@ SYMBOLS = (
     "w4_nf4_codebook", "w4_quantize_nf4", "w4_quantize_int4", "w4_dequantize_nf4",
     "w4_dequantize_int4", "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_workspace_bytes", "w4_step_create",
     "w4_step_launch", "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check",
-    "w4_launch_count", "w4_inject_timeout_once",
+    "w4_launch_count", "w4_inject_timeout_once", "w4_gemv_levels_noalloc",
 )
 
 
@@ -88,6 +91,7 @@ def _declare(L):
         "w4_device_check": (I, [P]),
         "w4_launch_count": (ctypes.c_longlong, []),
         "w4_inject_timeout_once": (I, []),
+        "w4_gemv_levels_noalloc": (I, [ctypes.POINTER(GemvDesc), I, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

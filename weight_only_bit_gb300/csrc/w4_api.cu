@@ -287,6 +287,25 @@ int w4_step_create(const w4_gemv_desc* descs, int count, void* workspace, w4_ste
   return W4_OK;
 }
 
+int w4_gemv_levels_noalloc(const w4_gemv_desc* descs, int count, w4_stream_t stream) {
+  int s = check_descs(descs, count);
+  if (s != W4_OK) return s;
+  const int nlevels = descs[count - 1].level + 1;
+  if (count > W4_NOALLOC_MAX_GEMVS || nlevels > W4_NOALLOC_MAX_LEVELS || nlevels > w4::noalloc_max_levels())
+    return W4_ERR_LIMIT;
+  if (!step_is_persistent(descs, count)) return W4_ERR_UNSUPPORTED;
+  w4::StepJob jobs[W4_NOALLOC_MAX_GEMVS];
+  for (int i = 0; i < count; ++i) {
+    const w4_gemv_desc& d = descs[i];
+    jobs[i] = w4::StepJob{d.packed, d.scales, reinterpret_cast<const __half*>(d.x), reinterpret_cast<__half*>(d.y),
+                          d.N, d.K, d.blocksize, d.level};
+  }
+  cudaError_t e = w4::launch_step_simt_noalloc(descs[0].format, jobs, count, descs[0].M, descs[0].codebook, nlevels,
+                                               reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return W4_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
 int w4_step_launch(w4_step* step, w4_stream_t stream) {
   if (!step || !step->exec) return W4_ERR_NULL;
   cudaError_t e = cudaGraphLaunch(step->exec, reinterpret_cast<cudaStream_t>(stream));
@@ -312,6 +331,7 @@ const char* w4_status_str(int status) {
     case W4_ERR_CUDA: return "CUDA runtime error";
     case W4_ERR_TIMEOUT: return "device-side wait timed out";
     case W4_ERR_UNSUPPORTED: return "unsupported by this build";
+    case W4_ERR_LIMIT: return "beyond the fixed counter array of w4_gemv_levels_noalloc (256 levels, 256 GEMVs)";
     default: return "unknown status";
   }
 }

@@ -53,4 +53,9 @@ struct StepJob {
 cudaError_t launch_step_simt(int format, const StepJob* jobs, int n, int M, const float* codebook, unsigned* counters,
                              bool pdl, cudaStream_t stream);
 
+// The same launch with the level counters in a fixed array inside the library (no caller memory).
+int noalloc_max_levels();
+cudaError_t launch_step_simt_noalloc(int format, const StepJob* jobs, int n, int M, const float* codebook,
+                                     int nlevels, cudaStream_t stream);
+
 }  // namespace w4

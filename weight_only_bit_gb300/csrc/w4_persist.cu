@@ -28,6 +28,8 @@
 // Every wait is bounded in wall-clock time; a lost wait is recorded in the device error word and
 // the kernel runs to its end without further waiting.
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -549,6 +551,46 @@ cudaError_t launch_step_simt(int format, const StepJob* jobs, int n, int M, cons
     js[i] = Job{jobs[i].packed, jobs[i].scales, jobs[i].x, jobs[i].y, jobs[i].N, jobs[i].K, jobs[i].bs, jobs[i].level};
   }
   return dispatch<kStepMaxGemvs, kStepMaxGemvs>(format, batch_block(M), js, n, M, codebook, counters, pdl, stream);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Counters for w4_gemv_levels_noalloc: a fixed array inside the library, for callers that cannot
+// allocate device memory.  In host code the name g_noalloc_counters is only a stand-in for the
+// device object; its device address is looked up once per device and cached.
+constexpr int kNoAllocMaxLevels = 256;
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) unsigned int g_noalloc_counters[kNoAllocMaxLevels + 1];
+
+static cudaError_t noalloc_counters(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  static std::mutex mu;
+  static unsigned* addr[kMaxDevices] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_counters);   // with this device current
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+int noalloc_max_levels() { return kNoAllocMaxLevels; }
+
+cudaError_t launch_step_simt_noalloc(int format, const StepJob* jobs, int n, int M, const float* codebook,
+                                     int nlevels, cudaStream_t stream) {
+  if (nlevels < 1 || nlevels > kNoAllocMaxLevels) return cudaErrorInvalidValue;
+  unsigned* counters = nullptr;
+  cudaError_t e = noalloc_counters(&counters);
+  if (e != cudaSuccess) return e;
+  // the array keeps the previous call's contents: start from zero
+  e = cudaMemsetAsync(counters, 0, sizeof(unsigned) * (size_t)(nlevels + 1), stream);
+  if (e != cudaSuccess) return e;
+  return launch_step_simt(format, jobs, n, M, codebook, counters, true, stream);
 }
 
 unsigned int read_clear_error_gemv() {
