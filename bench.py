@@ -228,7 +228,9 @@ class _GraphRunner:
             fn()
 
     def launch(self, stream):
-        self.g.replay()
+        import torch
+        with torch.cuda.stream(stream):     # replay on the stream the timing events are recorded on
+            self.g.replay()
         return 0
 
 

@@ -165,6 +165,25 @@ def test_gemv_parity(dev, fmt, m, n, k, bs):
     assert_gemv_close(y.cpu().numpy(), oracle_gemv(fmt, p_ref, s_ref, x, bs))
 
 
+TC_CASES = [
+    # (fmt, M, N, K, bs): the tensor-core path (batch >= 32), ragged rows and batches, split-K
+    ("nf4", 32, 8960, 1536, 64), ("nf4", 32, 1536, 8960, 64), ("nf4", 33, 257, 1536, 64), ("nf4", 64, 129, 512, 32),
+    ("nf4", 100, 300, 1536, 128), ("nf4", 128, 1536, 1536, 64), ("nf4", 128, 70, 8960, 256),
+    ("int4", 32, 8960, 1536, 128), ("int4", 32, 1536, 8960, 128), ("int4", 47, 257, 1536, 64),
+    ("int4", 128, 1536, 1536, 128), ("int4", 96, 130, 8960, 32),
+]
+
+
+@pytest.mark.parametrize("fmt,m,n,k,bs", TC_CASES)
+def test_tensor_core_batches(dev, fmt, m, n, k, bs):
+    w = synth.weights(8000 + n + k + m, n, k, outlier_frac=0.001)
+    x = synth.activations(8100 + n + k + m, m, k)
+    rows = np.unique(np.concatenate([[0, n - 1], np.random.default_rng(m).integers(0, n, 96)]))
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    y = gpu_gemv(fmt, _t(p_ref, dev), _t(s_ref, dev), x, n, k, bs, dev).cpu().numpy()
+    assert_gemv_close(y[:, rows], oracle_gemv(fmt, p_ref, s_ref, x, bs, rows=rows))
+
+
 @pytest.mark.parametrize("fmt", ["nf4", "int4"])
 @pytest.mark.parametrize("m", [12, 20, 32, 64, 128])
 def test_gemv_parity_larger_batches(dev, fmt, m):

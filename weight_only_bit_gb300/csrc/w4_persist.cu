@@ -289,9 +289,12 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) w4_persistent_kernel(co
       asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
     }
     int g = lv.gemv0;
+    PGemv gm = p.gm[g];
     for (int t = t_first; t < lv.tile0 + lv.ntiles; t += G, ++j) {
-      while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
-      const PGemv gm = p.gm[g];
+      if (t >= gm.tile0 + gm.ntiles) {
+        do { ++g; } while (t >= p.gm[g].tile0 + p.gm[g].ntiles);
+        gm = p.gm[g];
+      }
       if (gm.x != x_loaded || gm.K != k_loaded) {
         const int cpr = gm.cpr;
         rps = cpr >= kTargetConsumers ? 1 : kTargetConsumers / cpr;
