@@ -44,7 +44,7 @@ def peaks():
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("w4_gemv.cu", "w4_common.cuh"):
+    for f in ("w4_persist.cu", "w4_decode.cuh", "w4_common.cuh"):
         h.update(open(os.path.join(ROOT, "weight_only_bit_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
