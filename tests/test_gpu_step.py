@@ -102,3 +102,79 @@ def test_step_timeout_path_recovers(dev):
     assert w4.w4_device_check(stream) == 0
     _check_step(step, rows_per_gemv=16, seed=2)
     step.close()
+
+
+@pytest.mark.parametrize("fmt,batch", [("nf4", 1), ("int4", 1), ("nf4", 3), ("int4", 8)])
+def test_chained_levels_read_previous_outputs(dev, fmt, batch):
+    """A chain in ONE persistent launch where level L+1's x IS level L's y (written by other CTAs
+    during the same launch), with a fan-out level (two GEMVs on one x) and a long-K level.  Equal
+    bit for bit to one launch per GEMV (stream order), and every level within tolerance of the
+    oracle applied to the x the GPU actually read."""
+    code = oracle.nf4_codebook()
+    bs = 64 if fmt == "nf4" else 128
+    # (N, K) per GEMV and its level; level 3 has two GEMVs reading level 2's output
+    shapes = [(1536, 1536, 0), (2048, 1536, 1), (1536, 2048, 2), (640, 1536, 3), (1536, 1536, 3)]
+    codebook = torch.tensor(code, dtype=torch.float32, device=dev)
+    x0 = torch.from_numpy(synth.activations(777, batch, 1536)).to(dev)
+    ys, packs, scales, ws = [], [], [], []
+    for i, (n, k, lev) in enumerate(shapes):
+        w = synth.weights(5000 + i, n, k, outlier_frac=0.001)
+        ws.append(w)
+        W = torch.from_numpy(w).to(dev)
+        p = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
+        if fmt == "nf4":
+            s = torch.empty((n, k // bs), dtype=torch.float32, device=dev)
+            w4.check(w4.w4_quantize_nf4(W, p, s, codebook, n, k, bs))
+        else:
+            s = torch.empty((n, k // bs), dtype=torch.float16, device=dev)
+            w4.check(w4.w4_quantize_int4(W, p, s, n, k, bs))
+        packs.append(p)
+        scales.append(s)
+        ys.append(torch.full((batch, n), float("nan"), dtype=torch.float16, device=dev))
+    # level 0 reads x0; GEMV i > 0 reads the output of the last GEMV of the level before
+    xs = [x0, ys[0], ys[1], ys[2], ys[2]]
+    fmt_id = w4._lib.W4_FMT_NF4 if fmt == "nf4" else w4._lib.W4_FMT_INT4
+    descs = [dict(format=fmt_id, packed=packs[i], scales=scales[i], codebook=codebook, x=xs[i], y=ys[i],
+                  M=batch, N=n, K=k, blocksize=bs, level=lev) for i, (n, k, lev) in enumerate(shapes)]
+    torch.cuda.synchronize()
+    ws_bytes = w4.w4_step_workspace_bytes(len(descs))
+    workspace = torch.zeros(ws_bytes // 4, dtype=torch.int32, device=dev)
+    st, h = w4.w4_step_create(descs, workspace)
+    w4.check(st, "step create")
+    stream = torch.cuda.Stream(dev)
+    l0 = w4.w4_launch_count()
+    w4.check(w4.w4_step_launch(h, stream))
+    torch.cuda.synchronize()
+    assert w4.w4_launch_count() - l0 == 1
+    assert w4.w4_device_check(stream) == 0
+    got = [y.clone() for y in ys]
+    # each level against the oracle, fed the x the GPU read
+    for i, (n, k, lev) in enumerate(shapes):
+        x = xs[i].cpu().numpy().astype(np.float64)
+        if fmt == "nf4":
+            p, s = oracle.quantize_nf4(ws[i], code, bs)
+            y_ref = oracle.gemv_nf4(p, s, code, x, bs)
+        else:
+            p, s = oracle.quantize_int4(ws[i], bs)
+            y_ref = oracle.gemv_int4(p, s, x, bs)
+        y = got[i].cpu().numpy().astype(np.float64)
+        rms = np.sqrt(np.mean(y_ref ** 2, axis=1, keepdims=True))
+        assert np.all(np.abs(y - y_ref) <= 2e-2 * rms), i
+        rel = np.linalg.norm(y - y_ref, axis=1) / np.linalg.norm(y_ref, axis=1)
+        assert np.all(rel <= 1e-3), (i, rel)
+    # one launch per GEMV in stream order gives the same bits
+    for y in ys:
+        y.fill_(float("nan"))
+    w4.check(w4.w4_gemv_sequence(descs, stream))
+    torch.cuda.synchronize()
+    for a, b in zip(got, ys):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # and replays of the step keep giving them
+    for _ in range(3):
+        w4.check(w4.w4_step_launch(h, stream))
+    torch.cuda.synchronize()
+    assert w4.w4_device_check(stream) == 0
+    for a, b in zip(got, ys):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.all(workspace == 0)
+    w4.check(w4.w4_step_destroy(h))

@@ -37,10 +37,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
-// x read through L2 only: it may have been written by another SM earlier in the same launch.
-__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+// x: a plain (weak, L1-cached) load.  x may have been written by another SM earlier in the same
+// launch; the reader's CTA acquired that writer's release before any thread loads x, which makes
+// the write visible to these loads.  Every thread of a CTA reads its slice directly: L1 merges the
+// copies that threads sharing a chunk request, so L2 sees each line about once per SM.
+__device__ __forceinline__ uint4 ld_x_v4(const void* p) {
   uint4 v;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
 
@@ -84,8 +87,9 @@ struct XSlice {
   int s8[MB];
 };
 
-// x: FROM_SMEM ? this CTA's shared-memory copy of x : x in global memory (read through L2).
-template <int FMT, int MB, bool FROM_SMEM>
+// Loads the slice of x at `chunk` (32 elements) for batch rows m < M (zeros above M); x is row-major
+// [M][K] in global memory.
+template <int FMT, int MB>
 __device__ __forceinline__ void load_x_slice(XSlice<FMT, MB>& xs, const __half* __restrict__ x, int M, int K,
                                              int chunk) {
 #pragma unroll
@@ -95,7 +99,7 @@ __device__ __forceinline__ void load_x_slice(XSlice<FMT, MB>& xs, const __half* 
       const uint8_t* src = reinterpret_cast<const uint8_t*>(x + (size_t)m * K + (size_t)chunk * 32);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        uint4 q = FROM_SMEM ? *reinterpret_cast<const uint4*>(src + 16 * i) : ld_cg_v4(src + 16 * i);
+        const uint4 q = ld_x_v4(src + 16 * i);
         h[4 * i + 0] = q.x; h[4 * i + 1] = q.y; h[4 * i + 2] = q.z; h[4 * i + 3] = q.w;
       }
     } else {
@@ -108,102 +112,116 @@ __device__ __forceinline__ void load_x_slice(XSlice<FMT, MB>& xs, const __half* 
       xs.f[m] = 1.0f;
       xs.s8[m] = 0;
     } else {
-      float xf[32];
-      float mx = 0.0f;
+      // E: mx < 2^E with mx = max |x| (frexp's exponent; E = 0 for mx = 0), from the FP32 bits
+      __half2 amax = __habs2(*reinterpret_cast<const __half2*>(&h[0]));
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        __half2 hh = *reinterpret_cast<__half2*>(&h[i]);
-        float2 f2 = __half22float2(hh);
-        xf[2 * i] = f2.x;
-        xf[2 * i + 1] = f2.y;
-        mx = fmaxf(mx, fmaxf(fabsf(f2.x), fabsf(f2.y)));
-      }
-      int E = 0;
-      (void)frexpf(mx, &E);                 // mx < 2^E (mx == 0 gives E = 0)
-      const float up = ldexpf(1.0f, 15 - E);
+      for (int i = 1; i < 16; ++i) amax = __hmax2(amax, __habs2(*reinterpret_cast<const __half2*>(&h[i])));
+      const float mx = fmaxf(__low2float(amax), __high2float(amax));
+      const int E = mx > 0.0f ? (int)(__float_as_uint(mx) >> 23) - 126 : 0;
+      const float up = __uint_as_float((uint32_t)(127 + 15 - E) << 23);   // 2^(15 - E)
+      // X = rint(x * 2^(15-E)): the product is exact, and adding 1.5 * 2^23 in the same FMA rounds
+      // it to the nearest integer (ties to even), left in the low mantissa bits
       int X[32];
       int sx = 0;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        X[e] = __float2int_rn(xf[e] * up);  // |X| <= 32752
-        sx += X[e];
+      for (int i = 0; i < 16; ++i) {
+        const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+        X[2 * i] = (int)(__float_as_uint(fmaf(f2.x, up, 12582912.0f)) - 0x4B400000u);
+        X[2 * i + 1] = (int)(__float_as_uint(fmaf(f2.y, up, 12582912.0f)) - 0x4B400000u);
+        sx += X[2 * i] + X[2 * i + 1];
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        uint32_t ho = 0, lo = 0, he = 0, le = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int eo = 8 * i + 2 * b + 1, ee = 8 * i + 2 * b;
-          ho |= (uint32_t)((X[eo] >> 8) & 0xff) << (8 * b);
-          lo |= (uint32_t)(X[eo] & 0xff) << (8 * b);
-          he |= (uint32_t)((X[ee] >> 8) & 0xff) << (8 * b);
-          le |= (uint32_t)(X[ee] & 0xff) << (8 * b);
-        }
-        xs.v[m][4 * i + 0] = ho;
-        xs.v[m][4 * i + 1] = lo;
-        xs.v[m][4 * i + 2] = he;
-        xs.v[m][4 * i + 3] = le;
+        // 16-bit pairs, then the high and low bytes of four odd (low-nibble) and four even elements
+        uint32_t po01, po23, pe01, pe23;
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(po01) : "r"(X[8 * i + 1]), "r"(X[8 * i + 3]));
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(po23) : "r"(X[8 * i + 5]), "r"(X[8 * i + 7]));
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(pe01) : "r"(X[8 * i + 0]), "r"(X[8 * i + 2]));
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(pe23) : "r"(X[8 * i + 4]), "r"(X[8 * i + 6]));
+        asm("prmt.b32 %0, %1, %2, 0x7531;" : "=r"(xs.v[m][4 * i + 0]) : "r"(po01), "r"(po23));
+        asm("prmt.b32 %0, %1, %2, 0x6420;" : "=r"(xs.v[m][4 * i + 1]) : "r"(po01), "r"(po23));
+        asm("prmt.b32 %0, %1, %2, 0x7531;" : "=r"(xs.v[m][4 * i + 2]) : "r"(pe01), "r"(pe23));
+        asm("prmt.b32 %0, %1, %2, 0x6420;" : "=r"(xs.v[m][4 * i + 3]) : "r"(pe01), "r"(pe23));
       }
-      xs.f[m] = ldexpf(1.0f, E - 15);
+      xs.f[m] = __uint_as_float((uint32_t)(127 + E - 15) << 23);       // 2^(E - 15)
       xs.s8[m] = 8 * sx;
     }
   }
 }
 
-// One chunk of one row: part[m] = sum over the chunk's 32 weights of w_hat * x[m].
-// wv: the chunk's 16 packed bytes; scale_addr: shared-memory address of the row's scale for the
-// chunk (FP32 absmax for NF4, FP16 s for INT4); lut_lane: this lane's table base (NF4).
-template <int FMT, int MB>
-__device__ __forceinline__ void chunk_dot(float (&part)[MB], const uint4 wv, uint32_t scale_addr, uint32_t lut_lane,
-                                          const XSlice<FMT, MB>& xs) {
-  const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+// One chunk of R rows (R = 1 or 2, decoded together so their shared-memory reads overlap):
+// part[r][m] = sum over the chunk's 32 weights of w_hat[r] * x[m].  wv[r]: the chunk's 16 packed
+// bytes of row r; scale_addr[r]: shared-memory address of row r's scale for the chunk (FP32 absmax
+// for NF4, FP16 s for INT4); lut_lane: this lane's table base (NF4).
+template <int FMT, int MB, int R>
+__device__ __forceinline__ void chunk_dot(float (&part)[R][MB], const uint4 (&wv)[R], const uint32_t (&scale_addr)[R],
+                                          uint32_t lut_lane, const XSlice<FMT, MB>& xs) {
   if (FMT == 0) {
-    const float a = __uint_as_float(lds32(scale_addr));
-    constexpr int NA = MB >= 4 ? 1 : 4 / MB;   // independent accumulators per batch row
-    float acc[MB][NA];
+    float a[R];
 #pragma unroll
-    for (int m = 0; m < MB; ++m)
+    for (int r = 0; r < R; ++r) a[r] = __uint_as_float(lds32(scale_addr[r]));
+    constexpr int NA = MB >= 4 ? 1 : 4 / MB;   // independent accumulators per (row, batch row)
+    float acc[R][MB][NA];
 #pragma unroll
-      for (int q = 0; q < NA; ++q) acc[m][q] = 0.0f;
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int m = 0; m < MB; ++m)
+#pragma unroll
+        for (int q = 0; q < NA; ++q) acc[r][m][q] = 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+      uint32_t c2[R][4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        uint32_t byte;
-        asm("prmt.b32 %0, %1, 0, %2;" : "=r"(byte) : "r"(w4[i]), "r"(0x4440 + b));
-        const uint32_t c2 = lds32(lut_lane + byte * 128u);
+      for (int r = 0; r < R; ++r) {
+        const uint32_t w = i == 0 ? wv[r].x : i == 1 ? wv[r].y : i == 2 ? wv[r].z : wv[r].w;
 #pragma unroll
-        for (int m = 0; m < MB; ++m) mixed_dot2(acc[m][(4 * i + b) % NA], c2, xs.v[m][4 * i + b]);
+        for (int b = 0; b < 4; ++b) {
+          uint32_t byte;
+          asm("prmt.b32 %0, %1, 0, %2;" : "=r"(byte) : "r"(w), "r"(0x4440 + b));
+          c2[r][b] = lds32(lut_lane + byte * 128u);
+        }
       }
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+#pragma unroll
+          for (int m = 0; m < MB; ++m) mixed_dot2(acc[r][m][(4 * i + b) % NA], c2[r][b], xs.v[m][4 * i + b]);
     }
 #pragma unroll
-    for (int m = 0; m < MB; ++m) {
-      float s = 0.0f;
-#pragma unroll
-      for (int q = 0; q < NA; ++q) s += acc[m][q];
-      part[m] = s * a;
-    }
-  } else {
-    const float s = __half2float(__ushort_as_half((unsigned short)lds_u16(scale_addr)));
-    int ah[MB], al[MB];
-#pragma unroll
-    for (int m = 0; m < MB; ++m) { ah[m] = 0; al[m] = 0; }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = w4[i] & 0x0f0f0f0fu;
-      const uint32_t hi = (w4[i] >> 4) & 0x0f0f0f0fu;
+    for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int m = 0; m < MB; ++m) {
-        ah[m] = dp4a_us(lo, xs.v[m][4 * i + 0], ah[m]);
-        al[m] = dp4a_uu(lo, xs.v[m][4 * i + 1], al[m]);
-        ah[m] = dp4a_us(hi, xs.v[m][4 * i + 2], ah[m]);
-        al[m] = dp4a_uu(hi, xs.v[m][4 * i + 3], al[m]);
-      }
-    }
+        float sum = 0.0f;
 #pragma unroll
-    for (int m = 0; m < MB; ++m) {
-      const int tot = ah[m] * 256 + al[m] - xs.s8[m];
-      part[m] = (float)tot * (s * xs.f[m]);
+        for (int q = 0; q < NA; ++q) sum += acc[r][m][q];
+        part[r][m] = sum * a[r];
+      }
+  } else {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float s = __half2float(__ushort_as_half((unsigned short)lds_u16(scale_addr[r])));
+      const uint32_t w4[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+      int ah[MB], al[MB];
+#pragma unroll
+      for (int m = 0; m < MB; ++m) { ah[m] = 0; al[m] = 0; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = w4[i] & 0x0f0f0f0fu;
+        const uint32_t hi = (w4[i] >> 4) & 0x0f0f0f0fu;
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+          ah[m] = dp4a_us(lo, xs.v[m][4 * i + 0], ah[m]);
+          al[m] = dp4a_uu(lo, xs.v[m][4 * i + 1], al[m]);
+          ah[m] = dp4a_us(hi, xs.v[m][4 * i + 2], ah[m]);
+          al[m] = dp4a_uu(hi, xs.v[m][4 * i + 3], al[m]);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        const int tot = ah[m] * 256 + al[m] - xs.s8[m];
+        part[r][m] = (float)tot * (s * xs.f[m]);
+      }
     }
   }
 }

@@ -13,18 +13,28 @@
 // decode step's data dependencies ("Do Quantization and Sparsity make LLM Inference Faster ?",
 // section "What we did": the 197 GEMVs of one step).  Level 0 waits for the previous kernel in the
 // stream (programmatic dependent launch); later levels wait on tile counters in global memory.
-// Tile t of a level goes to CTA t mod gridDim.x; the grid is sized to be co-resident.
+// Tile t of a level goes to CTA t mod gridDim.x; the grid is one CTA per SM, all co-resident.
 //
 // Roles in a CTA:
-//   * producer warp: streams each tile's packed bytes and scales into a 3-stage shared-memory ring
-//     with 1-D bulk async copies (TMA unit), mbarrier completion, an L2 evict-first hint; it runs
-//     ahead across level boundaries (weights never depend on other GEMVs);
-//   * consumer warps: thread (rho, chunk) owns one 32-weight column chunk, keeps that slice of x in
-//     registers for the whole level, and produces one partial sum per (row, chunk);
-//   * reducer warp: sums each row's partials in a fixed order (lanes over chunks, then a warp
-//     shuffle: the reduction idiom of "Do Quantization and Sparsity make LLM Inference Faster ?",
-//     "Optional: what does the custom kernel actually do?"), writes y, and publishes tile
-//     completion; partial buffers are double-buffered, so consumers never wait for a reduction.
+//   * producer warp: streams each tile's packed bytes and scales into a shared-memory ring of up to
+//     eight stages with 1-D bulk async copies (TMA unit), mbarrier completion and an L2 evict-first
+//     hint.  Weights never depend on other GEMVs, so it runs ahead across level boundaries and
+//     prefetches later levels.  It issues copies only while its consumers compute (a stream gate
+//     opened once a level's x is loaded and closed when the CTA's last tile of the level is
+//     reduced): DRAM traffic during the grid-wide wait between levels multiplies that wait.  At
+//     most three copies are in flight, which already saturates DRAM;
+//   * consumer warps: thread (rho, chunk) owns one 32-weight column chunk, loads that slice of x
+//     (through L1, which merges the requests of the threads sharing it) into registers for the
+//     whole level, and produces one partial sum per (row, chunk), two rows at a time, into one of
+//     two partial-sum buffers;
+//   * reducer warp: sums each row's partials in a fixed order (eight interleaved sequences, then a
+//     fixed tree, over 1, 2, 4 or 8 lanes per row with warp shuffles: the reduction idiom of "Do
+//     Quantization and Sparsity make LLM Inference Faster ?", "Optional: what does the custom
+//     kernel actually do?"), writes y, and after the CTA's last tile of a level publishes
+//     completion with one release.  The order depends only on K, so a row gets the same bits
+//     whatever the tiling.  Each lane issues a whole batch of loads before its first add: the
+//     shared-memory queue is long while consumers decode, so one round trip per tile, not one per
+//     partial, keeps the reducer ahead of the consumers.
 // Every wait is bounded in wall-clock time; a lost wait is recorded in the device error word and
 // the kernel runs to its end without further waiting.
 #include <cstdint>
@@ -39,11 +49,27 @@
 
 namespace w4 {
 
-constexpr int kStages = 3;
-constexpr int kMaxConsumers = 320;      // consumer threads: one per chunk of a row x rows per sweep
-constexpr int kTargetConsumers = 288;
-constexpr int kStageTarget = 12288;     // packed bytes per stage (about)
-constexpr int kXCap = 18432;            // largest x (M x K x 2 bytes) staged in shared memory
+constexpr int kMaxStages = 8;
+constexpr int kMaxInFlight = 3;         // copies outstanding per CTA: enough for full DRAM bandwidth
+constexpr int kMaxConsumers = 320;      // longest row served: 320 chunks (K = 10240)
+constexpr int kStageTarget = 32768;     // packed bytes per stage (about)
+constexpr int kRedBufs = 2;             // partial-sum buffers: the reducer may lag one tile
+constexpr int kRedCapFloats = 8192;     // largest partial-sum buffer (floats)
+constexpr int kSmemCap = 227 * 1024;
+
+// Consumer warps per CTA by batch block: as many as the registers of one SM allow.
+__host__ __device__ constexpr int cons_warps(int MB) { return MB <= 1 ? 18 : MB == 2 ? 16 : 10; }
+
+// Lanes of the reducer warp per output row: all of a tile's outputs in one pass when possible.
+__host__ __device__ inline int red_lanes(int outs) {
+  int q = 8;
+  while (q > 1 && outs * q > 32) q >>= 1;
+  return q;
+}
+
+// Row stride (floats) of a partial-sum buffer: at least cpr and an odd multiple of Q, so the
+// (row, lane) reads of one reducer pass fall in 32 distinct banks.
+__host__ __device__ inline int red_stride(int cpr, int Q) { return cpr + ((Q - cpr) & (2 * Q - 1)); }
 
 struct PGemv {
   const uint8_t* packed;
@@ -64,32 +90,29 @@ struct PParams {
   const float* codebook;
   unsigned int* counters;  // [nlevels + 1] when nlevels > 1, else null
   int nlevels, ngemvs, M, inject_timeout;
-  int stage_w, stage_s, red_floats, n_consumer_warps;
-  int x_bytes;             // shared-memory x buffer (0: every thread reads its x slice from L2)
+  int stages, stage_w, stage_s, red_floats, n_consumer_warps;
   PLevel lv[MAXL];
   PGemv gm[MAXG];
 };
 
 struct PLayout {
-  int lut, x, w, s, red, bar, total;
+  int lut, w, s, red, bar, total;
 };
 
-__host__ __device__ inline PLayout playout(int fmt, int stage_w, int stage_s, int red_floats, int x_bytes) {
+__host__ __device__ inline PLayout playout(int fmt, int stages, int stage_w, int stage_s, int red_floats) {
   PLayout L;
   int off = 0;
   L.lut = 0;
   if (fmt == 0) off += kLutBytes;
-  L.x = off;
-  off += x_bytes;
   L.w = off;
-  off += kStages * stage_w;
+  off += stages * stage_w;
   L.s = off;
-  off += kStages * stage_s;
+  off += stages * stage_s;
   L.red = off;
-  off += 2 * red_floats * 4;
+  off += kRedBufs * red_floats * 4;
   off = (off + 15) & ~15;
   L.bar = off;
-  off += (2 * kStages + 4) * 8;
+  off += (2 * kMaxStages + 2 * kRedBufs) * 8 + 16;   // ring and buffer barriers, then the gate
   L.total = off;
   return L;
 }
@@ -106,42 +129,128 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-// Bounded wait until *p >= target (other CTAs' releases).  Records `site` on timeout.
+// Adds v with release semantics at GPU scope: every write ordered before it (this thread's, and
+// its warp's through a preceding __syncwarp) is visible to a thread that acquires the new value.
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until *p >= target (other CTAs' releases).  Polls back to back for the first
+// 20 microseconds, then backs off.  Records `site` on timeout.
 __device__ __forceinline__ bool wait_counter(const unsigned* p, unsigned target, uint32_t site) {
   if (ld_acquire_u32(p) >= target) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    __nanosleep(128);
     if (ld_acquire_u32(p) >= target) return true;
+    const uint64_t dt = globaltimer_ns() - t0;
+    if (dt > kWaitLimitNs) break;
+    if (dt > 20000) __nanosleep(256);
+  }
+  atomicCAS(&g_error_word, 0u, site);
+  return false;
+}
+
+// Bounded wait until the stream gate is open.
+__device__ __forceinline__ bool wait_gate(volatile int* gate, uint32_t site) {
+  if (*gate) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (*gate) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) break;
   }
   atomicCAS(&g_error_word, 0u, site);
   return false;
 }
 
+// Sum of one row's cpr partials rr[0 .. cpr) in the fixed order: sequence i (i < 8) adds
+// rr[i], rr[i + 8], rr[i + 16], ... from zero; the eight sums combine as
+// ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)).  Q lanes share the row (lane q holds the
+// sequences q, q + Q, ...); every lane of the group returns the same value, bit for bit, for any Q.
+// Loads go out in batches of 48 per lane before the adds that consume them.
+template <int Q>
+__device__ __forceinline__ float reduce_row(const float* rr, int cpr, int q) {
+  constexpr int U = 8 / Q;
+  constexpr int R = 48 / U;    // rounds of eight partials per batch
+  float a[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) a[u] = 0.0f;
+  int c0 = 0;
+  for (; c0 + 8 * R <= cpr; c0 += 8 * R) {   // full batches
+    float v[R][U];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[r][u] = rr[c0 + 8 * r + q + Q * u];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int u = 0; u < U; ++u) a[u] += v[r][u];
+  }
+  if (c0 < cpr) {                             // the ragged last batch
+    float v[R][U];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = c0 + 8 * r + q + Q * u;
+        v[r][u] = i < cpr ? rr[i] : 0.0f;
+      }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (c0 + 8 * r + q + Q * u < cpr) a[u] += v[r][u];
+      }
+  }
+  if constexpr (Q == 1) {
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+  } else {
+    // pairs (s0 + s1), (s2 + s3), ...: the partner sequence is one lane away
+#pragma unroll
+    for (int u = 0; u < U; ++u) a[u] += __shfl_xor_sync(0xffffffffu, a[u], 1);
+    if constexpr (Q == 2) {
+      return (a[0] + a[1]) + (a[2] + a[3]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) a[u] += __shfl_xor_sync(0xffffffffu, a[u], 2);
+      if constexpr (Q == 4) {
+        return a[0] + a[1];
+      } else {
+        return a[0] + __shfl_xor_sync(0xffffffffu, a[0], 4);
+      }
+    }
+  }
+}
+
 template <int FMT, int MB, int MAXL, int MAXG>
-__global__ void __launch_bounds__(kMaxConsumers + 64, 1) w4_persistent_kernel(const __grid_constant__ PParams<MAXL, MAXG> p) {
+__global__ void __launch_bounds__((cons_warps(MB) + 2) * 32, 1)
+    w4_persistent_kernel(const __grid_constant__ PParams<MAXL, MAXG> p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const PLayout Lo = playout(FMT, p.stage_w, p.stage_s, p.red_floats, p.x_bytes);
+  const PLayout Lo = playout(FMT, p.stages, p.stage_w, p.stage_s, p.red_floats);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lo.bar);
-  uint64_t* empty = full + kStages;
-  uint64_t* rfull = empty + kStages;
-  uint64_t* rfree = rfull + 2;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* rfull = empty + kMaxStages;
+  uint64_t* rfree = rfull + kRedBufs;
+  // stream gate: 1 while this CTA's consumers compute, 0 while they wait for the previous level
+  volatile int* gate = reinterpret_cast<volatile int*>(rfree + kRedBufs);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int ncw = p.n_consumer_warps;
   const int n_cons = ncw * 32;
   const int G = (int)gridDim.x;
+  const int NS = p.stages;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], ncw);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kRedBufs; ++i) {
       mbar_init(&rfull[i], ncw);
       mbar_init(&rfree[i], 1);
     }
+    *gate = 1;
     fence_mbar_init();
   }
   __syncthreads();
@@ -159,12 +268,17 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) w4_persistent_kernel(co
       for (int t = first_owned(lv.tile0); t < lv.tile0 + lv.ntiles; t += G, ++j) {
         while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
         const PGemv gm = p.gm[g];
-        const int st = j % kStages;
-        const int round = j / kStages;
-        // Prefetch of the first kStages tiles may overlap the previous kernel in the stream; the
+        const int st = j % NS;
+        const int round = j / NS;
+        // Prefetch of the first NS tiles may overlap the previous kernel in the stream; the
         // bounded waits start only once that kernel is complete.
         if (round == 1 && st == 0) pdl_wait();
         if (lane == 0 && round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1, 0x201);
+        if (lane == 0 && ok) ok = wait_gate(gate, 0x20a);
+        if (lane == 0 && NS > kMaxInFlight && j >= kMaxInFlight && ok) {
+          const int jd = j - kMaxInFlight;
+          ok = mbar_wait(&full[jd % NS], (jd / NS) & 1, 0x209);
+        }
         const int r0 = (t - gm.tile0) * gm.rpt;
         const int nrows = min(gm.rpt, gm.N - r0);
         const uint32_t wbytes = (uint32_t)nrows * (uint32_t)(gm.K / 2);
@@ -188,7 +302,7 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) w4_persistent_kernel(co
     }
     // never leave while bulk copies into this CTA's shared memory may be in flight
     if (lane == 0) {
-      for (int k = (j > kStages ? j - kStages : 0); k < j; ++k) mbar_wait(&full[k % kStages], (k / kStages) & 1, 0x202);
+      for (int k = (j > NS ? j - NS : 0); k < j; ++k) mbar_wait(&full[k % NS], (k / NS) & 1, 0x202);
     }
     return;
   }
@@ -207,42 +321,37 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) w4_persistent_kernel(co
       for (int t = first_owned(lv.tile0); t < t_end; t += G, ++j) {
         while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
         const PGemv gm = p.gm[g];
-        const int b = j & 1;
-        if (lane == 0 && ok) ok = mbar_wait(&rfull[b], (j >> 1) & 1, 0x203);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        const int b = j % kRedBufs;
+        if (ok) ok = mbar_wait(&rfull[b], (j / kRedBufs) & 1, 0x203);
         const int r0 = (t - gm.tile0) * gm.rpt;
         const int nrows = min(gm.rpt, gm.N - r0);
         const float* red = red_base + b * p.red_floats;
-        // one lane per output (row x batch row); each row sums its partials in one fixed order that
-        // depends only on K (eight interleaved accumulators, then a fixed tree), so a row gets the
-        // same bits whatever the tiling
+        // output o = m * nrows + lr is buffer row o; Q lanes per output
         const int outs = nrows * MB;
-        const int stride = gm.cpr + 1;             // odd row stride: conflict-free column reads
-        for (int o = lane; o < outs; o += 32) {
-          const int m = o / nrows;
-          const int lr = o - m * nrows;
-          const float* rr = red + (m * gm.rpt + lr) * stride;
-          float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          int c = 0;
-          for (; c + 7 < gm.cpr; c += 8) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a[i] += rr[c + i];
+        const int Q = red_lanes(outs);
+        const int stride = red_stride(gm.cpr, Q);
+        const int q = lane & (Q - 1);
+        for (int o0 = 0; o0 < outs; o0 += 32 / Q) {
+          const int o = o0 + lane / Q;
+          const int oc = o < outs ? o : outs - 1;
+          const float* rr = red + oc * stride;
+          float v;
+          switch (Q) {
+            case 8: v = reduce_row<8>(rr, gm.cpr, q); break;
+            case 4: v = reduce_row<4>(rr, gm.cpr, q); break;
+            case 2: v = reduce_row<2>(rr, gm.cpr, q); break;
+            default: v = reduce_row<1>(rr, gm.cpr, q); break;
           }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            if (c + i < gm.cpr) a[i] += rr[c + i];
-          }
-          const float v = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-          if (m < p.M) gm.y[(size_t)m * gm.N + r0 + lr] = __float2half_rn(v);
+          const int m = oc / nrows;
+          if (o < outs && q == 0 && m < p.M) gm.y[(size_t)m * gm.N + r0 + (oc - m * nrows)] = __float2half_rn(v);
         }
         const bool publish = p.counters && t + G >= t_end;   // this CTA's last tile of level L
-        if (publish) __threadfence();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&rfree[b]);
           if (publish) {
-            __threadfence();
-            atomicAdd(&p.counters[L], 1u);
+            if (L + 1 < p.nlevels) *gate = 0;   // before the release: the next level reopens it
+            red_release_add(&p.counters[L], 1u);
           }
         }
       }
@@ -263,8 +372,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) w4_persistent_kernel(co
   const int tid = threadIdx.x;
   const uint32_t lut_lane = smem_u32(smem + Lo.lut) + (uint32_t)lane * 4u;
   if (FMT == 0) build_nf4_lut(reinterpret_cast<uint32_t*>(smem + Lo.lut), p.codebook, tid, n_cons);
-  asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
 
+  constexpr int kTarget = cons_warps(MB) * 32;
   XSlice<FMT, MB> xs;
   const __half* x_loaded = nullptr;
   int k_loaded = -1;
@@ -276,7 +385,8 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) w4_persistent_kernel(co
   for (int L = 0; L < p.nlevels; ++L) {
     const PLevel lv = p.lv[L];
     const int t_first = first_owned(lv.tile0);
-    if (t_first >= lv.tile0 + lv.ntiles) continue;           // no tile of this level here
+    const int t_end = lv.tile0 + lv.ntiles;
+    if (t_first >= t_end) continue;           // no tile of this level here
     // ---- wait until this level's inputs exist
     if (!pdl_done) {
       pdl_wait();
@@ -286,60 +396,63 @@ __global__ void __launch_bounds__(kMaxConsumers + 64, 1) w4_persistent_kernel(co
       // every CTA that owns a tile of level L-1 adds one when it has finished them all
       const unsigned owners = (unsigned)min(G, p.lv[L - 1].ntiles);
       if (tid == 0 && ok) ok = wait_counter(&p.counters[L - 1], owners, 0x204);
-      asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
     }
+    // the level's start for all consumers (and the LUT complete at the first level): thread 0's
+    // acquire orders every consumer's reads of x after the previous level's writes
+    asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
     int g = lv.gemv0;
     PGemv gm = p.gm[g];
-    for (int t = t_first; t < lv.tile0 + lv.ntiles; t += G, ++j) {
+    for (int t = t_first; t < t_end; t += G, ++j) {
       if (t >= gm.tile0 + gm.ntiles) {
         do { ++g; } while (t >= p.gm[g].tile0 + p.gm[g].ntiles);
         gm = p.gm[g];
       }
       if (gm.x != x_loaded || gm.K != k_loaded) {
         const int cpr = gm.cpr;
-        rps = cpr >= kTargetConsumers ? 1 : kTargetConsumers / cpr;
+        rps = cpr >= kTarget ? 1 : kTarget / cpr;
         rho = tid / cpr;
         chunk = tid - rho * cpr;
         active = rho < rps;
-        const int xb = p.M * gm.K * 2;
-        if (xb <= p.x_bytes) {
-          // one coalesced copy of x per CTA (16-byte pieces through L2), then each thread takes
-          // its slice from shared memory: every SM reads x once instead of once per thread
-          __half* xsm = reinterpret_cast<__half*>(smem + Lo.x);
-          asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");    // previous x no longer read
-          for (int i = tid; i < xb / 16; i += n_cons) {
-            reinterpret_cast<uint4*>(xsm)[i] = ld_cg_v4(reinterpret_cast<const uint8_t*>(gm.x) + 16 * i);
-          }
-          asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
-          if (active) load_x_slice<FMT, MB, true>(xs, xsm, p.M, gm.K, chunk);
-        } else if (active) {
-          load_x_slice<FMT, MB, false>(xs, gm.x, p.M, gm.K, chunk);
-        }
+        if (active) load_x_slice<FMT, MB>(xs, gm.x, p.M, gm.K, chunk);
         x_loaded = gm.x;
         k_loaded = gm.K;
       }
-      const int st = j % kStages;
-      const int b = j & 1;
-      // lane 0 of each warp polls, the warp follows
-      if (lane == 0) {
-        if (ok) ok = mbar_wait(&full[st], (j / kStages) & 1, 0x205);
-        if (j >= 2 && ok) ok = mbar_wait(&rfree[b], ((j >> 1) - 1) & 1, 0x206);
-      }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (t == t_first && tid == 0) *gate = 1;
+      const int st = j % NS;
+      const int b = j % kRedBufs;
+      // every lane waits for itself: one instruction per warp, no broadcast round trip
+      if (ok) ok = mbar_wait(&full[st], (j / NS) & 1, 0x205);
+      if (j >= kRedBufs && ok) ok = mbar_wait(&rfree[b], ((j / kRedBufs) - 1) & 1, 0x206);
       const int r0 = (t - gm.tile0) * gm.rpt;
       const int nrows = min(gm.rpt, gm.N - r0);
       const uint32_t sw = smem_u32(smem + Lo.w + st * p.stage_w);
       const uint32_t ss = smem_u32(smem + Lo.s + st * p.stage_s);
       float* red = red_base + b * p.red_floats;
+      const int stride = red_stride(gm.cpr, red_lanes(nrows * MB));
       if (active && ok) {
         const int es = FMT == 0 ? 4 : 2;
         const uint32_t soff = (uint32_t)(((chunk * 32) / gm.bs) * es);
-        for (int lr = rho; lr < nrows; lr += rps) {
-          const uint4 wv = lds128(sw + (uint32_t)(lr * (gm.K / 2) + chunk * 16));
-          float part[MB];
-          chunk_dot<FMT, MB>(part, wv, ss + (uint32_t)(lr * gm.srb) + soff, lut_lane, xs);
+        const uint32_t wrow = (uint32_t)(gm.K / 2);
+        int lr = rho;
+        for (; lr + rps < nrows; lr += 2 * rps) {   // two rows at once
+          const uint4 wv[2] = {lds128(sw + (uint32_t)lr * wrow + chunk * 16),
+                               lds128(sw + (uint32_t)(lr + rps) * wrow + chunk * 16)};
+          const uint32_t sa[2] = {ss + (uint32_t)(lr * gm.srb) + soff, ss + (uint32_t)((lr + rps) * gm.srb) + soff};
+          float part[2][MB];
+          chunk_dot<FMT, MB, 2>(part, wv, sa, lut_lane, xs);
 #pragma unroll
-          for (int m = 0; m < MB; ++m) red[(m * gm.rpt + lr) * (gm.cpr + 1) + chunk] = part[m];
+          for (int m = 0; m < MB; ++m) {
+            red[(m * nrows + lr) * stride + chunk] = part[0][m];
+            red[(m * nrows + lr + rps) * stride + chunk] = part[1][m];
+          }
+        }
+        if (lr < nrows) {
+          const uint4 wv[1] = {lds128(sw + (uint32_t)lr * wrow + chunk * 16)};
+          const uint32_t sa[1] = {ss + (uint32_t)(lr * gm.srb) + soff};
+          float part[1][MB];
+          chunk_dot<FMT, MB, 1>(part, wv, sa, lut_lane, xs);
+#pragma unroll
+          for (int m = 0; m < MB; ++m) red[(m * nrows + lr) * stride + chunk] = part[0][m];
         }
       }
       __syncwarp();
@@ -372,24 +485,38 @@ static int gcd_int(int a, int b) {
 
 static int batch_block(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
 
+// Partial-sum floats a tile of nr rows needs.
+static int red_floats_for(int MB, int cpr, int nr) {
+  const int outs = nr * MB;
+  return outs * red_stride(cpr, red_lanes(outs));
+}
+
 // Per-GEMV geometry that does not depend on the tiling.
 struct GeomG {
-  int cpr, srb, align_rows, rpt_max, ncw, rps;
+  int cpr, srb, align_rows, rpt_max, ncw, rps, red_need;
 };
 
-static bool geom(int fmt, int K, int bs, GeomG& o) {
+static bool geom(int fmt, int MB, int K, int bs, GeomG& o) {
   o.cpr = K / 32;
   if (o.cpr < 1 || o.cpr > kMaxConsumers) return false;
-  const int rps = o.cpr >= kTargetConsumers ? 1 : kTargetConsumers / o.cpr;
+  const int target = cons_warps(MB) * 32;
+  const int rps = o.cpr >= target ? 1 : target / o.cpr;
   o.ncw = (rps * o.cpr + 31) / 32;
   o.srb = (K / bs) * (fmt == 0 ? 4 : 2);
   o.align_rows = 16 / gcd_int(o.srb, 16);       // keeps every tile's scale span 16-byte aligned
-  // about kStageTarget packed bytes, rounded to a whole number of consumer sweeps
+  o.rps = rps;
+  // about kStageTarget packed bytes, rounded to a whole number of consumer sweeps, within the
+  // partial-sum buffer's cap
   const int r = kStageTarget / (K / 2);
   int sweeps = (r + rps / 2) / rps;
   if (sweeps < 1) sweeps = 1;
-  o.rps = rps;
-  o.rpt_max = ((sweeps * rps + o.align_rows - 1) / o.align_rows) * o.align_rows;
+  int rows = sweeps * rps;
+  while (rows > 1 && red_floats_for(MB, o.cpr, rows) > kRedCapFloats) rows = rows > rps ? rows - rps : rows - 1;
+  rows = (rows / o.align_rows) * o.align_rows;
+  if (rows < o.align_rows) rows = o.align_rows;
+  o.rpt_max = rows;
+  o.red_need = 1;
+  for (int nr = 1; nr <= rows; ++nr) o.red_need = max(o.red_need, red_floats_for(MB, o.cpr, nr));
   return true;
 }
 
@@ -401,30 +528,35 @@ struct Job {
   int N, K, bs, level;
 };
 
-// Layout of a set of GEMVs at batch block MB (independent of tiling, which never exceeds rpt_max).
-static bool plan_layout(int fmt, int MB, int M, const Job* jobs, int n, int& stage_w, int& stage_s,
-                        int& red_floats, int& ncw, int& x_bytes, PLayout& L) {
-  stage_w = 16; stage_s = 16; red_floats = 1; ncw = 1; x_bytes = 0;
+struct Plan {
+  int stages, stage_w, stage_s, red_floats, ncw;
+  PLayout L;
+};
+
+// Layout of a set of GEMVs at batch block MB (independent of tiling, which never exceeds rpt_max):
+// the fixed parts, then as many ring stages (2 ... kMaxStages) as shared memory holds.
+static bool plan_layout(int fmt, int MB, int M, const Job* jobs, int n, Plan& P) {
+  P.stage_w = 16; P.stage_s = 16; P.red_floats = 1; P.ncw = 1;
   for (int i = 0; i < n; ++i) {
     GeomG gg;
-    if (!geom(fmt, jobs[i].K, jobs[i].bs, gg)) return false;
-    stage_w = max(stage_w, gg.rpt_max * (jobs[i].K / 2));
-    stage_s = max(stage_s, ((gg.rpt_max * gg.srb) + 15) & ~15);
-    red_floats = max(red_floats, MB * gg.rpt_max * (gg.cpr + 1));
-    ncw = max(ncw, gg.ncw);
-    const int xb = M * jobs[i].K * 2;
-    if (xb <= kXCap) x_bytes = max(x_bytes, xb);
+    if (!geom(fmt, MB, jobs[i].K, jobs[i].bs, gg)) return false;
+    P.stage_w = max(P.stage_w, gg.rpt_max * (jobs[i].K / 2));
+    P.stage_s = max(P.stage_s, ((gg.rpt_max * gg.srb) + 15) & ~15);
+    P.red_floats = max(P.red_floats, gg.red_need);
+    P.ncw = max(P.ncw, gg.ncw);
   }
-  L = playout(fmt, stage_w, stage_s, red_floats, x_bytes);
-  return L.total <= 227 * 1024;
+  for (P.stages = kMaxStages; P.stages >= 2; --P.stages) {
+    P.L = playout(fmt, P.stages, P.stage_w, P.stage_s, P.red_floats);
+    if (P.L.total <= kSmemCap) return true;
+  }
+  return false;
 }
 
 int simt_max_batch(int format, int K, int bs) {
   Job jb{nullptr, nullptr, nullptr, nullptr, 1, K, bs, 0};
   for (int m : {8, 4, 2, 1}) {
-    int sw, ss, rf, ncw, xb;
-    PLayout L;
-    if (plan_layout(format, m, m, &jb, 1, sw, ss, rf, ncw, xb, L)) return m;
+    Plan P;
+    if (plan_layout(format, m, m, &jb, 1, P)) return m;
   }
   return 0;
 }
@@ -439,25 +571,24 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
   int nlev = 0;
   for (int i = 0; i < n; ++i) nlev = max(nlev, jobs[i].level + 1);
   if (n > MAXG || nlev > MAXL) { delete pp; return cudaErrorNotSupported; }
-  int stage_w, stage_s, red_floats, ncw, x_bytes;
-  PLayout L;
-  if (!plan_layout(FMT, MB, M, jobs, n, stage_w, stage_s, red_floats, ncw, x_bytes, L)) {
+  Plan plan;
+  if (!plan_layout(FMT, MB, M, jobs, n, plan)) {
     delete pp;
     return cudaErrorNotSupported;
   }
   static bool attr_done = false;   // one flag per instance
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
     if (e != cudaSuccess) { delete pp; return e; }
     attr_done = true;
   }
-  const int threads = ncw * 32 + 64;
+  const int threads = plan.ncw * 32 + 64;
   static int occ_threads = -1, occ_smem = -1, occ_val = 1;
-  if (occ_threads != threads || occ_smem != L.total) {
+  if (occ_threads != threads || occ_smem != plan.L.total) {
     int v = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, (size_t)L.total);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, (size_t)plan.L.total);
     if (e != cudaSuccess) { delete pp; return e; }
-    occ_threads = threads; occ_smem = L.total; occ_val = v < 1 ? 1 : (v > 2 ? 2 : v);
+    occ_threads = threads; occ_smem = plan.L.total; occ_val = v < 1 ? 1 : (v > 2 ? 2 : v);
   }
   const int gmax = device_sm_count() * occ_val;
   p.codebook = codebook;
@@ -467,8 +598,8 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
   p.ngemvs = n;
   p.M = M;
   p.inject_timeout = take_fault_injection();
-  p.stage_w = stage_w; p.stage_s = stage_s; p.red_floats = red_floats; p.n_consumer_warps = ncw;
-  p.x_bytes = x_bytes;
+  p.stages = plan.stages; p.stage_w = plan.stage_w; p.stage_s = plan.stage_s; p.red_floats = plan.red_floats;
+  p.n_consumer_warps = plan.ncw;
   // tiling, level by level: balanced tiles per CTA, rows per tile within each GEMV's stage budget
   int tile = 0, max_level_tiles = 0;
   for (int Lv = 0, i = 0; Lv < nlev; ++Lv) {
@@ -477,7 +608,7 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
     int rmin = 1 << 30;
     while (i < n && jobs[i].level == Lv) {
       GeomG gg;
-      geom(FMT, jobs[i].K, jobs[i].bs, gg);
+      geom(FMT, MB, jobs[i].K, jobs[i].bs, gg);
       rows += jobs[i].N;
       rmin = min(rmin, gg.rpt_max);
       ++i;
@@ -488,7 +619,7 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
     const long long tpc = (rows + (long long)gmax * rmin - 1) / ((long long)gmax * rmin);
     for (int q = first; q < i; ++q) {
       GeomG gg;
-      geom(FMT, jobs[q].K, jobs[q].bs, gg);
+      geom(FMT, MB, jobs[q].K, jobs[q].bs, gg);
       int rpt = (int)((rows + (long long)gmax * tpc - 1) / ((long long)gmax * tpc));
       if (rpt > gg.rps) rpt = ((rpt + gg.rps - 1) / gg.rps) * gg.rps;   // whole sweeps when it can
       rpt = ((rpt + gg.align_rows - 1) / gg.align_rows) * gg.align_rows;
@@ -506,7 +637,7 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3((unsigned)threads);
-  cfg.dynamicSmemBytes = (size_t)L.total;
+  cfg.dynamicSmemBytes = (size_t)plan.L.total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
