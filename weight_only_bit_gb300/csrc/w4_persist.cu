@@ -52,7 +52,8 @@ namespace w4 {
 constexpr int kMaxStages = 8;
 constexpr int kMaxInFlight = 3;         // copies outstanding per CTA: enough for full DRAM bandwidth
 constexpr int kMaxConsumers = 320;      // longest row served: 320 chunks (K = 10240)
-constexpr int kStageTarget = 32768;     // packed bytes per stage (about)
+constexpr int kStageTarget = 65536;     // packed bytes per stage (about): large tiles amortise each
+                                        // tile's barrier round trips; smaller when the ring won't fit
 constexpr int kRedBufs = 2;             // partial-sum buffers: the reducer may lag one tile
 constexpr int kRedCapFloats = 8192;     // largest partial-sum buffer (floats)
 constexpr int kSmemCap = 227 * 1024;
@@ -496,7 +497,7 @@ struct GeomG {
   int cpr, srb, align_rows, rpt_max, ncw, rps, red_need;
 };
 
-static bool geom(int fmt, int MB, int K, int bs, GeomG& o) {
+static bool geom(int fmt, int MB, int K, int bs, int stage_target, GeomG& o) {
   o.cpr = K / 32;
   if (o.cpr < 1 || o.cpr > kMaxConsumers) return false;
   const int target = cons_warps(MB) * 32;
@@ -507,7 +508,7 @@ static bool geom(int fmt, int MB, int K, int bs, GeomG& o) {
   o.rps = rps;
   // about kStageTarget packed bytes, rounded to a whole number of consumer sweeps, within the
   // partial-sum buffer's cap
-  const int r = kStageTarget / (K / 2);
+  const int r = stage_target / (K / 2);
   int sweeps = (r + rps / 2) / rps;
   if (sweeps < 1) sweeps = 1;
   int rows = sweeps * rps;
@@ -529,25 +530,28 @@ struct Job {
 };
 
 struct Plan {
-  int stages, stage_w, stage_s, red_floats, ncw;
+  int stage_target, stages, stage_w, stage_s, red_floats, ncw;
   PLayout L;
 };
 
 // Layout of a set of GEMVs at batch block MB (independent of tiling, which never exceeds rpt_max):
-// the fixed parts, then as many ring stages (2 ... kMaxStages) as shared memory holds.
+// the fixed parts, then as many ring stages (2 ... kMaxStages) as shared memory holds; the stage
+// size steps down from kStageTarget until two stages fit.
 static bool plan_layout(int fmt, int MB, int M, const Job* jobs, int n, Plan& P) {
-  P.stage_w = 16; P.stage_s = 16; P.red_floats = 1; P.ncw = 1;
-  for (int i = 0; i < n; ++i) {
-    GeomG gg;
-    if (!geom(fmt, MB, jobs[i].K, jobs[i].bs, gg)) return false;
-    P.stage_w = max(P.stage_w, gg.rpt_max * (jobs[i].K / 2));
-    P.stage_s = max(P.stage_s, ((gg.rpt_max * gg.srb) + 15) & ~15);
-    P.red_floats = max(P.red_floats, gg.red_need);
-    P.ncw = max(P.ncw, gg.ncw);
-  }
-  for (P.stages = kMaxStages; P.stages >= 2; --P.stages) {
-    P.L = playout(fmt, P.stages, P.stage_w, P.stage_s, P.red_floats);
-    if (P.L.total <= kSmemCap) return true;
+  for (P.stage_target = kStageTarget; P.stage_target >= 2048; P.stage_target = P.stage_target * 3 / 4) {
+    P.stage_w = 16; P.stage_s = 16; P.red_floats = 1; P.ncw = 1;
+    for (int i = 0; i < n; ++i) {
+      GeomG gg;
+      if (!geom(fmt, MB, jobs[i].K, jobs[i].bs, P.stage_target, gg)) return false;
+      P.stage_w = max(P.stage_w, gg.rpt_max * (jobs[i].K / 2));
+      P.stage_s = max(P.stage_s, ((gg.rpt_max * gg.srb) + 15) & ~15);
+      P.red_floats = max(P.red_floats, gg.red_need);
+      P.ncw = max(P.ncw, gg.ncw);
+    }
+    for (P.stages = kMaxStages; P.stages >= 2; --P.stages) {
+      P.L = playout(fmt, P.stages, P.stage_w, P.stage_s, P.red_floats);
+      if (P.L.total <= kSmemCap) return true;
+    }
   }
   return false;
 }
@@ -608,7 +612,7 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
     int rmin = 1 << 30;
     while (i < n && jobs[i].level == Lv) {
       GeomG gg;
-      geom(FMT, MB, jobs[i].K, jobs[i].bs, gg);
+      geom(FMT, MB, jobs[i].K, jobs[i].bs, plan.stage_target, gg);
       rows += jobs[i].N;
       rmin = min(rmin, gg.rpt_max);
       ++i;
@@ -619,7 +623,7 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
     const long long tpc = (rows + (long long)gmax * rmin - 1) / ((long long)gmax * rmin);
     for (int q = first; q < i; ++q) {
       GeomG gg;
-      geom(FMT, MB, jobs[q].K, jobs[q].bs, gg);
+      geom(FMT, MB, jobs[q].K, jobs[q].bs, plan.stage_target, gg);
       int rpt = (int)((rows + (long long)gmax * tpc - 1) / ((long long)gmax * tpc));
       if (rpt > gg.rps) rpt = ((rpt + gg.rps - 1) / gg.rps) * gg.rps;   // whole sweeps when it can
       rpt = ((rpt + gg.align_rows - 1) / gg.align_rows) * gg.align_rows;
