@@ -153,6 +153,9 @@ GEMV_CASES = [
     ("int4", 1, 1536, 1536, 128), ("int4", 1, 100, 8960, 128), ("int4", 2, 333, 1536, 128), ("int4", 3, 64, 8960, 128),
     ("int4", 4, 1000, 1536, 128), ("int4", 5, 129, 1536, 128), ("int4", 8, 777, 1536, 128), ("int4", 8, 61, 8960, 128),
     ("int4", 1, 70, 512, 32), ("int4", 1, 70, 512, 64), ("int4", 2, 70, 1024, 256),
+    # an odd number of chunks per row and of batch rows x chunks (shared-memory layouts whose
+    # parts are not multiples of 16 bytes)
+    ("nf4", 1, 45, 96, 32), ("int4", 1, 45, 96, 32), ("int4", 3, 40, 160, 32), ("nf4", 3, 40, 160, 32),
 ]
 
 

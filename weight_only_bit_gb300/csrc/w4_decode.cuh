@@ -149,6 +149,42 @@ __device__ __forceinline__ void load_x_slice(XSlice<FMT, MB>& xs, const __half* 
   }
 }
 
+// INT4 digit table shared by the threads of a CTA: for chunk c of batch row m, its 16 digit words,
+// the factor and 8 * sum X at word (m * kXDigitWords + w) * cpr + c (a warp's accesses to one word
+// are contiguous: no bank conflict).
+constexpr int kXDigitWords = 18;
+
+template <int MB>
+__device__ __forceinline__ void put_x_digits(uint32_t* xd, const XSlice<1, MB>& xs, int M, int cpr, int chunk) {
+#pragma unroll
+  for (int m = 0; m < MB; ++m) {
+    if (m < M) {
+#pragma unroll
+      for (int w = 0; w < 16; ++w) xd[(m * kXDigitWords + w) * cpr + chunk] = xs.v[m][w];
+      xd[(m * kXDigitWords + 16) * cpr + chunk] = __float_as_uint(xs.f[m]);
+      xd[(m * kXDigitWords + 17) * cpr + chunk] = (uint32_t)xs.s8[m];
+    }
+  }
+}
+
+template <int MB>
+__device__ __forceinline__ void get_x_digits(XSlice<1, MB>& xs, const uint32_t* xd, int M, int cpr, int chunk) {
+#pragma unroll
+  for (int m = 0; m < MB; ++m) {
+    if (m < M) {
+#pragma unroll
+      for (int w = 0; w < 16; ++w) xs.v[m][w] = xd[(m * kXDigitWords + w) * cpr + chunk];
+      xs.f[m] = __uint_as_float(xd[(m * kXDigitWords + 16) * cpr + chunk]);
+      xs.s8[m] = (int)xd[(m * kXDigitWords + 17) * cpr + chunk];
+    } else {
+#pragma unroll
+      for (int w = 0; w < 16; ++w) xs.v[m][w] = 0u;
+      xs.f[m] = 1.0f;
+      xs.s8[m] = 0;
+    }
+  }
+}
+
 // One chunk of R rows (R = 1 or 2, decoded together so their shared-memory reads overlap):
 // part[r][m] = sum over the chunk's 32 weights of w_hat[r] * x[m].  wv[r]: the chunk's 16 packed
 // bytes of row r; scale_addr[r]: shared-memory address of row r's scale for the chunk (FP32 absmax

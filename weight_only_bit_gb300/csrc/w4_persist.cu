@@ -56,6 +56,7 @@ constexpr int kStageTarget = 65536;     // packed bytes per stage (about): large
                                         // tile's barrier round trips; smaller when the ring won't fit
 constexpr int kRedBufs = 2;             // partial-sum buffers: the reducer may lag one tile
 constexpr int kRedCapFloats = 8192;     // largest partial-sum buffer (floats)
+constexpr int kXDigitCap = 40960;       // largest INT4 x digit table shared in shared memory (bytes)
 constexpr int kSmemCap = 227 * 1024;
 
 // Consumer warps per CTA by batch block: as many as the registers of one SM allow.
@@ -92,19 +93,23 @@ struct PParams {
   unsigned int* counters;  // [nlevels + 1] when nlevels > 1, else null
   int nlevels, ngemvs, M, inject_timeout;
   int stages, stage_w, stage_s, red_floats, n_consumer_warps;
+  int xd_bytes;            // INT4: shared x digit table (0: every thread converts its slice)
   PLevel lv[MAXL];
   PGemv gm[MAXG];
 };
 
 struct PLayout {
-  int lut, w, s, red, bar, total;
+  int lut, xd, w, s, red, bar, total;
 };
 
-__host__ __device__ inline PLayout playout(int fmt, int stages, int stage_w, int stage_s, int red_floats) {
+__host__ __device__ inline PLayout playout(int fmt, int stages, int stage_w, int stage_s, int red_floats,
+                                           int xd_bytes) {
   PLayout L;
   int off = 0;
   L.lut = 0;
   if (fmt == 0) off += kLutBytes;
+  L.xd = off;
+  off += (xd_bytes + 15) & ~15;   // bulk copies into the ring need 16-byte alignment
   L.w = off;
   off += stages * stage_w;
   L.s = off;
@@ -228,7 +233,7 @@ template <int FMT, int MB, int MAXL, int MAXG>
 __global__ void __launch_bounds__((cons_warps(MB) + 2) * 32, 1)
     w4_persistent_kernel(const __grid_constant__ PParams<MAXL, MAXG> p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const PLayout Lo = playout(FMT, p.stages, p.stage_w, p.stage_s, p.red_floats);
+  const PLayout Lo = playout(FMT, p.stages, p.stage_w, p.stage_s, p.red_floats, p.xd_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lo.bar);
   uint64_t* empty = full + kMaxStages;
   uint64_t* rfull = empty + kMaxStages;
@@ -414,7 +419,22 @@ __global__ void __launch_bounds__((cons_warps(MB) + 2) * 32, 1)
         rho = tid / cpr;
         chunk = tid - rho * cpr;
         active = rho < rps;
-        if (active) load_x_slice<FMT, MB>(xs, gm.x, p.M, gm.K, chunk);
+        bool shared_digits = false;
+        if constexpr (FMT == 1) {
+          if (t == t_first && p.M * cpr * 4 * kXDigitWords <= p.xd_bytes) {
+            // INT4: the threads of one row sweep (rho == 0) convert each chunk of x once and share
+            // the digits; the level-start barrier above ordered every read of the previous table
+            shared_digits = true;
+            uint32_t* xd = reinterpret_cast<uint32_t*>(smem + Lo.xd);
+            if (rho == 0 && active) {
+              load_x_slice<FMT, MB>(xs, gm.x, p.M, gm.K, chunk);
+              put_x_digits<MB>(xd, xs, p.M, cpr, chunk);
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
+            if (rho > 0 && active) get_x_digits<MB>(xs, xd, p.M, cpr, chunk);
+          }
+        }
+        if (!shared_digits && active) load_x_slice<FMT, MB>(xs, gm.x, p.M, gm.K, chunk);
         x_loaded = gm.x;
         k_loaded = gm.K;
       }
@@ -530,7 +550,7 @@ struct Job {
 };
 
 struct Plan {
-  int stage_target, stages, stage_w, stage_s, red_floats, ncw;
+  int stage_target, stages, stage_w, stage_s, red_floats, ncw, xd_bytes;
   PLayout L;
 };
 
@@ -539,7 +559,7 @@ struct Plan {
 // size steps down from kStageTarget until two stages fit.
 static bool plan_layout(int fmt, int MB, int M, const Job* jobs, int n, Plan& P) {
   for (P.stage_target = kStageTarget; P.stage_target >= 2048; P.stage_target = P.stage_target * 3 / 4) {
-    P.stage_w = 16; P.stage_s = 16; P.red_floats = 1; P.ncw = 1;
+    P.stage_w = 16; P.stage_s = 16; P.red_floats = 1; P.ncw = 1; P.xd_bytes = 0;
     for (int i = 0; i < n; ++i) {
       GeomG gg;
       if (!geom(fmt, MB, jobs[i].K, jobs[i].bs, P.stage_target, gg)) return false;
@@ -547,9 +567,11 @@ static bool plan_layout(int fmt, int MB, int M, const Job* jobs, int n, Plan& P)
       P.stage_s = max(P.stage_s, ((gg.rpt_max * gg.srb) + 15) & ~15);
       P.red_floats = max(P.red_floats, gg.red_need);
       P.ncw = max(P.ncw, gg.ncw);
+      const int xd = M * gg.cpr * 4 * kXDigitWords;
+      if (fmt == 1 && xd <= kXDigitCap) P.xd_bytes = max(P.xd_bytes, xd);
     }
     for (P.stages = kMaxStages; P.stages >= 2; --P.stages) {
-      P.L = playout(fmt, P.stages, P.stage_w, P.stage_s, P.red_floats);
+      P.L = playout(fmt, P.stages, P.stage_w, P.stage_s, P.red_floats, P.xd_bytes);
       if (P.L.total <= kSmemCap) return true;
     }
   }
@@ -604,6 +626,7 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
   p.inject_timeout = take_fault_injection();
   p.stages = plan.stages; p.stage_w = plan.stage_w; p.stage_s = plan.stage_s; p.red_floats = plan.red_floats;
   p.n_consumer_warps = plan.ncw;
+  p.xd_bytes = plan.xd_bytes;
   // tiling, level by level: balanced tiles per CTA, rows per tile within each GEMV's stage budget
   int tile = 0, max_level_tiles = 0;
   for (int Lv = 0, i = 0; Lv < nlev; ++Lv) {
