@@ -42,6 +42,33 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak():
+    """Measured dense bf16 TFLOP/s (burst), the denominator for batch >= 32 contractions (FP16
+    operands have the same tensor rate)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def run_sweep(args):
+    """The batch sweep of the pages' small-batch configurations: every decode shape alone at batch
+    1, 8, 32 and 128, NF4 and INT4, weights N(0, 0.02) with 0.1 % outliers at 10 sigma.  One JSON
+    line; not part of the default run."""
+    import torch
+    from weight_only_bit_gb300 import build as _b
+    _b.build()
+    dev = torch.device("cuda:0")
+    hbm, _ = peaks()
+    tfp, tsrc = bf16_peak()
+    res = {}
+    for fmt in ("nf4", "int4"):
+        for M in (1, 8, 32, 128):
+            shapes, weighted = per_shape(fmt, dev, torch, hbm, M=M, tflops_peak=tfp, outlier_frac=0.001)
+            res[f"{fmt}_b{M}"] = {"shapes": shapes, "weighted_step_us": round(weighted, 2)}
+    print(json.dumps({"sweep": res, "hbm_peak_GB_s": hbm, "bf16_peak_TFLOP_s": tfp, "peak_source": tsrc}), flush=True)
+
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     for f in ("w4_persist.cu", "w4_decode.cuh", "w4_common.cuh"):
@@ -234,8 +261,8 @@ class _GraphRunner:
         return 0
 
 
-def per_shape(fmt, dev, torch, hbm):
-    """Each decode shape alone, batch 1: a chain of back-to-back launches (one per weight copy,
+def per_shape(fmt, dev, torch, hbm, M=1, tflops_peak=None, outlier_frac=0.0):
+    """Each decode shape alone at batch M: a chain of back-to-back launches (one per weight copy,
     distinct copies totalling > 4x L2, so every launch streams from HBM) replayed as a graph; the
     time per launch is what one such GEMV costs inside a launch-per-GEMV decode step."""
     import weight_only_bit_gb300 as w4
@@ -249,7 +276,7 @@ def per_shape(fmt, dev, torch, hbm):
         code = torch.tensor(c, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
     for name, n, k, _ in synth.DECODE_SHAPES:
-        w = synth.weights(synth.weight_seed(0 if name != "lm_head" else 28, name), n, k)
+        w = synth.weights(synth.weight_seed(0 if name != "lm_head" else 28, name), n, k, outlier_frac=outlier_frac)
         W = torch.from_numpy(w).to(dev)
         packed = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
         sdt = torch.float32 if fmt == "nf4" else torch.float16
@@ -263,19 +290,24 @@ def per_shape(fmt, dev, torch, hbm):
         copies = max(2, min(4096, (4 * 129 * 2 ** 20) // per + 1))
         P = packed.reshape(1, -1).repeat(copies, 1)
         S = sc.reshape(1, -1).repeat(copies, 1)
-        x = torch.from_numpy(synth.activations(synth.x_seed(0, synth.X_SLOT[name], 1), 1, k)).to(dev)
-        y = torch.empty((1, n), dtype=torch.float16, device=dev)
+        x = torch.from_numpy(synth.activations(synth.x_seed(0, synth.X_SLOT[name], M), M, k)).to(dev)
+        y = torch.empty((M, n), dtype=torch.float16, device=dev)
         descs = [dict(format=_lib.W4_FMT_NF4 if fmt == "nf4" else _lib.W4_FMT_INT4, packed=P[i], scales=S[i],
-                      codebook=code, x=x, y=y, M=1, N=n, K=k, blocksize=bs) for i in range(copies)]
+                      codebook=code, x=x, y=y, M=M, N=n, K=k, blocksize=bs) for i in range(copies)]
         arr = w4._descs(descs)
         lib = w4.lib()
         runner = _GraphRunner(torch, stream, lambda: w4.check(lib.w4_gemv_sequence(arr, len(descs),
                                                                                   stream.cuda_stream)))
         ms = time_graph(runner, stream, 5, 2, torch) / copies
-        nbytes = per + 2 * k + 2 * n
+        nbytes = per + 2 * M * k + 2 * M * n
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"N": n, "K": k, "us": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
                      "frac_of_measured": round(gbs / hbm, 4), "launches_timed": copies * 5}
+        if M >= 32:
+            tf = 2.0 * M * n * k / (ms * 1e-3) / 1e12
+            out[name]["TFLOP_s"] = round(tf, 1)
+            if tflops_peak:
+                out[name]["frac_of_bf16_peak"] = round(tf / tflops_peak, 4)
         del runner, P, S
         torch.cuda.empty_cache()
     # the pages' "weighted" step: sum over shapes of count x per-launch time
@@ -435,6 +467,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the INT4 step and the per-shape table")
+    ap.add_argument("--sweep", action="store_true", help="only the per-shape batch sweep (1, 8, 32, 128; NF4, INT4)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -442,6 +475,9 @@ def main():
         if int(os.environ.get("RANK", "0")) != 0:
             return
         run_reference(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     run_ours(args)
 

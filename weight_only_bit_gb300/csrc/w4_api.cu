@@ -67,6 +67,13 @@ int enqueue_gemv(int format, const uint8_t* packed, const void* scales, const fl
                  uint16_t* y, int M, int N, int K, int bs, cudaStream_t stream) {
   const __half* xh = reinterpret_cast<const __half*>(x);
   __half* yh = reinterpret_cast<__half*>(y);
+  // batches >= 16: the 5th-generation tensor cores (tcgen05).  Both tensor-core kernels need K to
+  // be a multiple of 64; the mma.sync one (batch >= 32) also serves if the TMA descriptors cannot
+  // be made.  Everything else runs on the CUDA cores.
+  if (M >= 16) {
+    cudaError_t e = w4::launch_gemv_tc5(format, packed, scales, codebook, xh, yh, M, N, K, bs, true, stream);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+  }
   if (M >= 32) {
     cudaError_t e = w4::launch_gemv_tc(format, packed, scales, codebook, xh, yh, M, N, K, bs, true, stream);
     if (e != cudaErrorNotSupported) return cuda_status(e);
