@@ -62,10 +62,11 @@ def run_sweep(args):
     hbm, _ = peaks()
     tfp, tsrc = bf16_peak()
     res = {}
-    for fmt in ("nf4", "int4"):
-        for M in (1, 8, 32, 128):
-            shapes, weighted = per_shape(fmt, dev, torch, hbm, M=M, tflops_peak=tfp, outlier_frac=0.001)
-            res[f"{fmt}_b{M}"] = {"shapes": shapes, "weighted_step_us": round(weighted, 2)}
+    only = set(args.sweep_shapes.split(",")) if args.sweep_shapes else None
+    for fmt in args.sweep_formats.split(","):
+        for M in (int(b) for b in args.sweep_batches.split(",")):
+            shapes, weighted = per_shape(fmt, dev, torch, hbm, M=M, tflops_peak=tfp, outlier_frac=0.001, only=only)
+            res[f"{fmt}_b{M}"] = {"shapes": shapes, "weighted_step_us": round(weighted, 2) if only is None else None}
     print(json.dumps({"sweep": res, "hbm_peak_GB_s": hbm, "bf16_peak_TFLOP_s": tfp, "peak_source": tsrc}), flush=True)
 
 
@@ -261,7 +262,7 @@ class _GraphRunner:
         return 0
 
 
-def per_shape(fmt, dev, torch, hbm, M=1, tflops_peak=None, outlier_frac=0.0):
+def per_shape(fmt, dev, torch, hbm, M=1, tflops_peak=None, outlier_frac=0.0, only=None):
     """Each decode shape alone at batch M: a chain of back-to-back launches (one per weight copy,
     distinct copies totalling > 4x L2, so every launch streams from HBM) replayed as a graph; the
     time per launch is what one such GEMV costs inside a launch-per-GEMV decode step."""
@@ -276,6 +277,8 @@ def per_shape(fmt, dev, torch, hbm, M=1, tflops_peak=None, outlier_frac=0.0):
         code = torch.tensor(c, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
     for name, n, k, _ in synth.DECODE_SHAPES:
+        if only is not None and name not in only:
+            continue
         w = synth.weights(synth.weight_seed(0 if name != "lm_head" else 28, name), n, k, outlier_frac=outlier_frac)
         W = torch.from_numpy(w).to(dev)
         packed = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
@@ -311,7 +314,7 @@ def per_shape(fmt, dev, torch, hbm, M=1, tflops_peak=None, outlier_frac=0.0):
         del runner, P, S
         torch.cuda.empty_cache()
     # the pages' "weighted" step: sum over shapes of count x per-launch time
-    weighted_us = sum(out[nm]["us"] * c for nm, _, _, c in synth.DECODE_SHAPES)
+    weighted_us = sum(out[nm]["us"] * c for nm, _, _, c in synth.DECODE_SHAPES if nm in out)
     return out, weighted_us
 
 
@@ -468,6 +471,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="skip the INT4 step and the per-shape table")
     ap.add_argument("--sweep", action="store_true", help="only the per-shape batch sweep (1, 8, 32, 128; NF4, INT4)")
+    ap.add_argument("--sweep-batches", default="1,8,32,128", help="batches of the sweep, comma-separated")
+    ap.add_argument("--sweep-formats", default="nf4,int4", help="formats of the sweep, comma-separated")
+    ap.add_argument("--sweep-shapes", default="", help="decode shapes of the sweep (default: all), comma-separated")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -118,7 +118,7 @@ int w4_dequantize_int4(const uint8_t* packed, const uint16_t* scale, float* W_ou
  * dequantised weight matrix is ever written ("LLM Quantization on RTX 4060", sections
  * "Fused Kernel: Moving Dequantization On-Chip" and "Kernel Implementation"; FP32
  * accumulation as that kernel's comment requires).  y is rounded to FP16 (nearest even).
- * Batches 1 ... 15 run on CUDA cores; batches 16 ... 128 on the 5th-generation tensor cores
+ * Batches 1 ... 8 run on CUDA cores; batches 9 ... 128 on the 5th-generation tensor cores
  * (tcgen05) when K is a multiple of 64, else on CUDA cores.
  * Sizes: 1 <= M <= W4_MAX_BATCH, N >= 1, 32 <= K <= W4_MAX_K, K % blocksize == 0,
  * blocksize a power of two in [32, 256].  packed, scales, x 16-byte aligned; y 2-byte aligned.

@@ -169,12 +169,12 @@ def test_gemv_parity(dev, fmt, m, n, k, bs):
 
 
 TC_CASES = [
-    # (fmt, M, N, K, bs): the tensor-core paths (batch >= 16), ragged rows and batches, split-K
+    # (fmt, M, N, K, bs): the tensor-core paths (batch >= 9), ragged rows and batches, split-K
     # over a cluster (few row tiles), persistent tiles (many), a partial last 256-k super-chunk,
     # and shapes the tcgen05 kernel does not take (K % 64 != 0: mma.sync or CUDA cores)
     ("nf4", 16, 256, 1536, 64), ("int4", 16, 1000, 1600, 32), ("nf4", 24, 200, 320, 64), ("int4", 20, 8960, 1536, 128),
     ("nf4", 17, 128, 64, 64), ("int4", 24, 1536, 8960, 128), ("nf4", 40, 100, 96, 32), ("int4", 20, 100, 160, 32),
-    ("int4", 128, 384, 768, 256), ("nf4", 64, 1536, 8960, 64),
+    ("int4", 128, 384, 768, 256), ("nf4", 64, 1536, 8960, 64), ("nf4", 9, 8960, 1536, 64), ("int4", 13, 300, 8960, 128),
     ("nf4", 32, 8960, 1536, 64), ("nf4", 32, 1536, 8960, 64), ("nf4", 33, 257, 1536, 64), ("nf4", 64, 129, 512, 32),
     ("nf4", 100, 300, 1536, 128), ("nf4", 128, 1536, 1536, 64), ("nf4", 128, 70, 8960, 256),
     ("int4", 32, 8960, 1536, 128), ("int4", 32, 1536, 8960, 128), ("int4", 47, 257, 1536, 64),

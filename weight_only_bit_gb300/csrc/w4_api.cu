@@ -67,10 +67,12 @@ int enqueue_gemv(int format, const uint8_t* packed, const void* scales, const fl
                  uint16_t* y, int M, int N, int K, int bs, cudaStream_t stream) {
   const __half* xh = reinterpret_cast<const __half*>(x);
   __half* yh = reinterpret_cast<__half*>(y);
-  // batches >= 16: the 5th-generation tensor cores (tcgen05).  Both tensor-core kernels need K to
-  // be a multiple of 64; the mma.sync one (batch >= 32) also serves if the TMA descriptors cannot
-  // be made.  Everything else runs on the CUDA cores.
-  if (M >= 16) {
+  // batches above 8: the 5th-generation tensor cores (tcgen05; a batch below 16 is padded to 16
+  // MMA columns at no extra MMA cost).  Batches up to 8 stay on the CUDA cores, whose arithmetic
+  // the persistent step kernel shares bit for bit.  Both tensor-core kernels need K to be a
+  // multiple of 64; the mma.sync one (batch >= 32) also serves if the TMA descriptors cannot be
+  // made.  Everything else runs on the CUDA cores.
+  if (M > 8) {
     cudaError_t e = w4::launch_gemv_tc5(format, packed, scales, codebook, xh, yh, M, N, K, bs, true, stream);
     if (e != cudaErrorNotSupported) return cuda_status(e);
   }

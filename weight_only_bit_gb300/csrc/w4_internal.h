@@ -27,7 +27,7 @@ cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scal
                              const __half* x, __half* y, int M, int N, int K, int bs, bool pdl,
                              cudaStream_t stream);
 
-// One GEMV on the 5th-generation tensor cores (tcgen05, batch 1 ... 128; used from batch 16).
+// One GEMV on the 5th-generation tensor cores (tcgen05, batch 1 ... 128; used from batch 9).
 // cudaErrorNotSupported when the shape is not one it takes (K % 64 != 0, unaligned bases).
 cudaError_t launch_gemv_tc5(int format, const uint8_t* packed, const void* scales, const float* codebook,
                             const __half* x, __half* y, int M, int N, int K, int bs, bool pdl,

@@ -1,7 +1,7 @@
 // w4_tc5.cu -- fused 4-bit dequant-GEMM on the 5th-generation tensor cores (tcgen05) for batches
-// 16 ... 128 (sm_103a).
+// 9 ... 128 (sm_103a).
 //
-// At these batches every decoded weight feeds 16-128 multiply-adds: the work is a dense
+// At these batches every decoded weight feeds 9-128 multiply-adds: the work is a dense
 // contraction and belongs on the tensor cores ("My Triton Kernel Ties bitsandbytes", section "Why
 // Marlin is still faster").  Weights are decoded on chip and never written back to DRAM ("LLM
 // Quantization on RTX 4060", section "Fused Kernel: Moving Dequantization On-Chip").
