@@ -133,6 +133,31 @@ int w4_gemv_int4(const uint8_t* packed, const uint16_t* scale,
                  w4_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * w4_gemv_plan -- which kernel w4_gemv_nf4 / w4_gemv_int4 would run for these sizes, and its
+ * launch geometry, on a GPU with sm_count SMs (152 on GB300).  The batch-driven choice of
+ * path is the one "Do Quantization and Sparsity make LLM Inference Faster ?" describes for
+ * bitsandbytes (section "NF4: fast at batch 1, slower at larger batches").  Host only: no
+ * device call, nothing allocated; *plan is caller-owned and fully written on W4_OK.
+ *   kernel      W4_KERNEL_CUDA_CORES or W4_KERNEL_TCGEN05
+ *   launches    kernel launches the call makes (CUDA cores: one per <= batch_tile rows)
+ *   batch_tile  batch rows per launch (CUDA cores) or MMA N columns (tcgen05: 16/32/64/128)
+ *   threads     threads per CTA; smem_bytes: dynamic shared memory per CTA
+ *   stages      ring stages (CUDA cores: packed tiles; tcgen05: x / A stages)
+ *   grid        CTAs per launch (tcgen05), or 0 where the launch sizes it from occupancy
+ *   cluster     CTAs per thread-block cluster splitting K (1: no split)
+ * For the CUDA cores the figures are those of the widest launch.  The mma.sync tensor-core
+ * kernel, which serves only if the driver cannot encode TMA descriptors, is not predicted.
+ * Errors: W4_ERR_NULL (plan NULL), W4_ERR_UNSUPPORTED (format, M > W4_MAX_BATCH or a shape
+ * no kernel takes), W4_ERR_SHAPE / W4_ERR_BLOCKSIZE as for the GEMV, W4_ERR_SHAPE for
+ * sm_count < 1.
+ */
+typedef enum { W4_KERNEL_CUDA_CORES = 1, W4_KERNEL_TCGEN05 = 2 } w4_kernel;
+typedef struct {
+  int kernel, launches, batch_tile, threads, smem_bytes, stages, grid, cluster;
+} w4_gemv_plan_t;
+int w4_gemv_plan(int format, int M, int N, int K, int blocksize, int sm_count, w4_gemv_plan_t* plan);
+
+/* ---------------------------------------------------------------------------------------
  * Decode step: the projections of one decode step ("Do Quantization and Sparsity make LLM
  * Inference Faster ?", section "What we did": 197 GEMVs per token).  Descriptors carry a level:
  * levels start at 0 and never decrease along the array; the GEMVs of one level are independent

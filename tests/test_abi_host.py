@@ -102,3 +102,96 @@ def test_status_strings(libw4):
     assert w4.w4_status_str(_lib.W4_ERR_ALIGN) != w4.w4_status_str(_lib.W4_ERR_SHAPE)
     with pytest.raises(w4.W4Error):
         w4.check(_lib.W4_ERR_SHAPE, "shape")
+
+
+# ---------------------------------------------------------------- dispatch and launch geometry
+# w4_gemv_plan is the host half of w4_gemv_nf4 / w4_gemv_int4's dispatch (the same functions
+# size the real launches), so these checks pin the batch-driven path choice and the tcgen05
+# kernel's resource use without a GPU.  152 SMs: a GB300.
+
+SMS = 152
+DECODE = {"q": (1536, 1536), "k": (256, 1536), "gate": (8960, 1536), "down": (1536, 8960), "lm_head": (151936, 1536)}
+
+
+def _plan(fmt, m, n, k, bs, sms=SMS):
+    st, p = w4.w4_gemv_plan(fmt, m, n, k, bs, sms)
+    assert st == w4.W4_OK, (fmt, m, n, k, bs, st)
+    return p
+
+
+@pytest.mark.parametrize("fmt,bs", [(w4.W4_FMT_NF4, 64), (w4.W4_FMT_INT4, 128)])
+def test_plan_batches_up_to_8_stay_on_cuda_cores(libw4, fmt, bs):
+    for m in range(1, 9):
+        for n, k in DECODE.values():
+            p = _plan(fmt, m, n, k, bs)
+            assert p["kernel"] == w4.W4_KERNEL_CUDA_CORES and p["launches"] == 1 and p["batch_tile"] == m
+            assert p["cluster"] == 1 and p["smem_bytes"] <= 227 * 1024 and p["stages"] >= 2
+
+
+@pytest.mark.parametrize("fmt,bs", [(w4.W4_FMT_NF4, 64), (w4.W4_FMT_INT4, 128), (w4.W4_FMT_NF4, 32),
+                                    (w4.W4_FMT_INT4, 256)])
+def test_plan_tcgen05_resources(libw4, fmt, bs):
+    for m in list(range(9, 129, 7)) + [16, 17, 32, 33, 64, 65, 128]:
+        for n, k in list(DECODE.values()) + [(1, 256), (129, 64), (300, 320), (70, 8960)]:
+            if k % bs:
+                continue
+            p = _plan(fmt, m, n, k, bs)
+            assert p["kernel"] == w4.W4_KERNEL_TCGEN05
+            nb = p["batch_tile"]
+            assert nb in (16, 32, 64, 128) and nb >= m and (nb == 16 or nb // 2 < m)
+            assert p["threads"] == 864 and p["launches"] == 1
+            assert p["smem_bytes"] <= 227 * 1024 and 4 <= p["stages"] <= 8
+            # tensor memory: two accumulators of max(32, NB) columns, then 32 columns per A stage
+            assert 2 * max(32, nb) <= 256 and 256 + 32 * p["stages"] <= 512
+            nrb = -(-n // 128)
+            if p["cluster"] > 1:
+                assert p["cluster"] <= 8 and p["cluster"] <= -(-k // 256)
+                assert p["grid"] == nrb * p["cluster"] <= SMS and 2 * nrb <= SMS
+                # the FP32 partial tile [128][NB + 4] fits in the x stages (NB x 128 bytes each)
+                assert 128 * (nb + 4) * 4 <= p["stages"] * nb * 128
+            else:
+                assert p["grid"] == min(nrb, SMS)
+
+
+def test_plan_split_choices_on_the_decode_shapes(libw4):
+    nf4 = w4.W4_FMT_NF4
+    # few row tiles and enough K: split over a cluster sized to cover the SMs
+    assert _plan(nf4, 32, *DECODE["q"], 64)["cluster"] == 6           # 12 tiles x 6 super-chunks
+    assert _plan(nf4, 32, *DECODE["q"], 64)["grid"] == 72
+    assert _plan(nf4, 16, *DECODE["k"], 64)["cluster"] == 6           # 2 tiles
+    assert _plan(nf4, 32, *DECODE["down"], 64)["cluster"] == 8        # 35 super-chunks, 8 at most
+    assert _plan(nf4, 128, *DECODE["down"], 64)["cluster"] == 8
+    # the split does not pay: gate at batch >= 32 (70 tiles, 2-way split), q at batch 128
+    assert _plan(nf4, 32, *DECODE["gate"], 64)["cluster"] == 1
+    assert _plan(nf4, 128, *DECODE["gate"], 64)["cluster"] == 1
+    assert _plan(nf4, 128, *DECODE["q"], 64)["cluster"] == 1
+    # many row tiles: persistent, one CTA per SM
+    p = _plan(nf4, 32, *DECODE["lm_head"], 64)
+    assert p["cluster"] == 1 and p["grid"] == SMS
+    # a one-super-chunk K cannot be split
+    assert _plan(nf4, 32, 128, 256, 64)["cluster"] == 1
+    # fewer SMs: smaller clusters, never more CTAs than SMs
+    p = _plan(nf4, 32, *DECODE["q"], 64, sms=36)
+    assert p["cluster"] == 3 and p["grid"] == 36
+
+
+def test_plan_shapes_the_tensor_cores_do_not_take(libw4):
+    # K not a multiple of 64: CUDA-core launches of at most 8 batch rows
+    p = _plan(w4.W4_FMT_NF4, 40, 100, 96, 32)
+    assert p["kernel"] == w4.W4_KERNEL_CUDA_CORES and p["launches"] == 5 and p["batch_tile"] == 8
+    p = _plan(w4.W4_FMT_INT4, 20, 100, 160, 32)
+    assert p["kernel"] == w4.W4_KERNEL_CUDA_CORES and p["launches"] == 3
+
+
+def test_plan_validation(libw4):
+    out = w4.GemvPlan()
+    ref = ctypes.byref(out)
+    assert libw4.w4_gemv_plan(0, 1, 16, 64, 64, SMS, None) == w4.W4_ERR_NULL
+    assert libw4.w4_gemv_plan(2, 1, 16, 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED
+    assert libw4.w4_gemv_plan(0, 0, 16, 64, 64, SMS, ref) == w4.W4_ERR_SHAPE
+    assert libw4.w4_gemv_plan(0, 129, 16, 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED
+    assert libw4.w4_gemv_plan(0, 1, 0, 64, 64, SMS, ref) == w4.W4_ERR_SHAPE
+    assert libw4.w4_gemv_plan(0, 1, 16, 96, 64, SMS, ref) == w4.W4_ERR_SHAPE
+    assert libw4.w4_gemv_plan(0, 1, 16, 96, 48, SMS, ref) == w4.W4_ERR_BLOCKSIZE
+    assert libw4.w4_gemv_plan(0, 1, 16, 64, 64, 0, ref) == w4.W4_ERR_SHAPE
+    assert libw4.w4_gemv_plan(0, 1, 16, w4.W4_MAX_K + 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED

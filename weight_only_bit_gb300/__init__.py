@@ -9,17 +9,18 @@ from __future__ import annotations
 
 import ctypes
 
-from ._lib import (GemvDesc, W4Error, lib, SYMBOLS, W4_OK, W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_ALIGN,
+from ._lib import (GemvDesc, GemvPlan, W4Error, lib, SYMBOLS, W4_OK, W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_ALIGN,
                    W4_ERR_BLOCKSIZE, W4_ERR_CUDA, W4_ERR_TIMEOUT, W4_ERR_UNSUPPORTED, W4_FMT_NF4,
-                   W4_FMT_INT4, W4_MAX_BATCH, W4_MAX_K)
+                   W4_FMT_INT4, W4_MAX_BATCH, W4_MAX_K, W4_KERNEL_CUDA_CORES, W4_KERNEL_TCGEN05)
 
 __all__ = [
     "w4_nf4_codebook", "w4_quantize_nf4", "w4_quantize_int4", "w4_dequantize_nf4", "w4_dequantize_int4",
     "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_workspace_bytes", "w4_step_create",
     "w4_step_launch",
     "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check", "w4_launch_count",
-    "w4_inject_timeout_once", "w4_gemv_levels_noalloc",
-    "check", "W4Error", "GemvDesc", "W4_FMT_NF4", "W4_FMT_INT4", "W4_MAX_BATCH", "W4_MAX_K",
+    "w4_inject_timeout_once", "w4_gemv_levels_noalloc", "w4_gemv_plan",
+    "check", "W4Error", "GemvDesc", "GemvPlan", "W4_FMT_NF4", "W4_FMT_INT4", "W4_MAX_BATCH", "W4_MAX_K",
+    "W4_KERNEL_CUDA_CORES", "W4_KERNEL_TCGEN05",
 ]
 
 
@@ -125,6 +126,13 @@ def w4_last_cuda_error() -> int:
 
 def w4_device_check(stream=None) -> int:
     return lib().w4_device_check(_stream(stream))
+
+
+def w4_gemv_plan(format: int, M: int, N: int, K: int, blocksize: int, sm_count: int = 152):
+    """Host function: returns (status, dict of w4_gemv_plan_t's fields); no device call."""
+    out = GemvPlan()
+    st = lib().w4_gemv_plan(format, M, N, K, blocksize, sm_count, ctypes.byref(out))
+    return st, {name: getattr(out, name) for name, _ in GemvPlan._fields_}
 
 
 def w4_launch_count() -> int:

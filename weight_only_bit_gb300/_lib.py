@@ -24,6 +24,8 @@ W4_NOALLOC_MAX_LEVELS = 256
 W4_NOALLOC_MAX_GEMVS = 256
 W4_FMT_NF4 = 0
 W4_FMT_INT4 = 1
+W4_KERNEL_CUDA_CORES = 1
+W4_KERNEL_TCGEN05 = 2
 W4_MAX_BATCH = 128
 W4_MAX_K = 10240
 
@@ -32,7 +34,7 @@ SYMBOLS = (
     "w4_nf4_codebook", "w4_quantize_nf4", "w4_quantize_int4", "w4_dequantize_nf4",
     "w4_dequantize_int4", "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_workspace_bytes", "w4_step_create",
     "w4_step_launch", "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check",
-    "w4_launch_count", "w4_inject_timeout_once", "w4_gemv_levels_noalloc",
+    "w4_launch_count", "w4_inject_timeout_once", "w4_gemv_levels_noalloc", "w4_gemv_plan",
 )
 
 
@@ -68,6 +70,12 @@ class GemvDesc(ctypes.Structure):
     ]
 
 
+class GemvPlan(ctypes.Structure):
+    """w4_gemv_plan_t of include/w4.h."""
+    _fields_ = [(name, ctypes.c_int) for name in
+                ("kernel", "launches", "batch_tile", "threads", "smem_bytes", "stages", "grid", "cluster")]
+
+
 _lib = None
 
 
@@ -92,6 +100,7 @@ def _declare(L):
         "w4_launch_count": (ctypes.c_longlong, []),
         "w4_inject_timeout_once": (I, []),
         "w4_gemv_levels_noalloc": (I, [ctypes.POINTER(GemvDesc), I, P]),
+        "w4_gemv_plan": (I, [I, I, I, I, I, I, ctypes.POINTER(GemvPlan)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

@@ -61,6 +61,10 @@ int check_gemv(int format, const uint8_t* packed, const void* scales, const floa
   return W4_OK;
 }
 
+// Batches above 8 go to the tcgen05 kernel (where it takes the shape); batches up to 8 stay on
+// the CUDA cores, whose arithmetic the persistent step kernel shares bit for bit.
+bool tc5_batch(int M) { return M > 8; }
+
 // Enqueue one validated GEMV.  Batches above one CUDA-core launch's budget are split into
 // launches over consecutive batch rows (each re-reads the weights).
 int enqueue_gemv(int format, const uint8_t* packed, const void* scales, const float* codebook, const uint16_t* x,
@@ -72,7 +76,7 @@ int enqueue_gemv(int format, const uint8_t* packed, const void* scales, const fl
   // the persistent step kernel shares bit for bit.  Both tensor-core kernels need K to be a
   // multiple of 64; the mma.sync one (batch >= 32) also serves if the TMA descriptors cannot be
   // made.  Everything else runs on the CUDA cores.
-  if (M > 8) {
+  if (tc5_batch(M)) {
     cudaError_t e = w4::launch_gemv_tc5(format, packed, scales, codebook, xh, yh, M, N, K, bs, true, stream);
     if (e != cudaErrorNotSupported) return cuda_status(e);
   }
@@ -207,6 +211,24 @@ static int check_descs(const w4_gemv_desc* descs, int count) {
     if (d.level < want_lo || d.level > (i == 0 ? 0 : prev_level + 1)) return W4_ERR_SHAPE;
     prev_level = d.level;
   }
+  return W4_OK;
+}
+
+int w4_gemv_plan(int format, int M, int N, int K, int blocksize, int sm_count, w4_gemv_plan_t* plan) {
+  if (!plan) return W4_ERR_NULL;
+  if (format != W4_FMT_NF4 && format != W4_FMT_INT4) return W4_ERR_UNSUPPORTED;
+  int s = check_shape(N, K, blocksize);
+  if (s != W4_OK) return s;
+  if (M < 1 || sm_count < 1) return W4_ERR_SHAPE;
+  if (M > W4_MAX_BATCH) return W4_ERR_UNSUPPORTED;
+  w4::Tc5Plan tp;
+  if (tc5_batch(M) && w4::plan_tc5(M, N, K, blocksize, sm_count, &tp)) {
+    *plan = w4_gemv_plan_t{W4_KERNEL_TCGEN05, 1, tp.nb, tp.threads, tp.smem, tp.ns, tp.grid, tp.ks};
+    return W4_OK;
+  }
+  w4::SimtPlan sp;
+  if (!w4::plan_simt(format, M, K, blocksize, &sp)) return W4_ERR_UNSUPPORTED;
+  *plan = w4_gemv_plan_t{W4_KERNEL_CUDA_CORES, sp.launches, sp.mb, sp.threads, sp.smem, sp.stages, 0, 1};
   return W4_OK;
 }
 

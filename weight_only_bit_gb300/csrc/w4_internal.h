@@ -27,6 +27,20 @@ cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scal
                              const __half* x, __half* y, int M, int N, int K, int bs, bool pdl,
                              cudaStream_t stream);
 
+// Launch geometry of the tcgen05 GEMV (host only): MMA batch columns, packed slots, x / A stages,
+// CTAs per cluster along K (1: persistent over row tiles), CTAs, threads, dynamic shared memory.
+struct Tc5Plan {
+  int nb, np, ns, ks, grid, threads, smem;
+};
+bool plan_tc5(int M, int N, int K, int bs, int sms, Tc5Plan* out);
+
+// CUDA-core launches of a batch-M GEMV (host only): rows of the widest launch, launches, and that
+// launch's threads, dynamic shared memory and ring stages.  False if the shape is unsupported.
+struct SimtPlan {
+  int mb, launches, threads, smem, stages;
+};
+bool plan_simt(int format, int M, int K, int bs, SimtPlan* out);
+
 // One GEMV on the 5th-generation tensor cores (tcgen05, batch 1 ... 128; used from batch 9).
 // cudaErrorNotSupported when the shape is not one it takes (K % 64 != 0, unaligned bases).
 cudaError_t launch_gemv_tc5(int format, const uint8_t* packed, const void* scales, const float* codebook,

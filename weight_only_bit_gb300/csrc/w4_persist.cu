@@ -587,6 +587,22 @@ int simt_max_batch(int format, int K, int bs) {
   return 0;
 }
 
+bool plan_simt(int format, int M, int K, int bs, SimtPlan* out) {
+  const int mb = simt_max_batch(format, K, bs);
+  if (mb < 1 || M < 1) return false;
+  // the widest launch: min(M, mb) rows on the batch block that covers them
+  const int mm = M < mb ? M : mb;
+  Job jb{nullptr, nullptr, nullptr, nullptr, 1, K, bs, 0};
+  Plan P;
+  if (!plan_layout(format, batch_block(mm), mm, &jb, 1, P)) return false;
+  out->mb = mm;
+  out->launches = (M + mb - 1) / mb;
+  out->threads = P.ncw * 32 + 64;
+  out->smem = P.L.total;
+  out->stages = P.stages;
+  return true;
+}
+
 template <int FMT, int MB, int MAXL, int MAXG>
 static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float* codebook, unsigned* counters,
                                      bool pdl, cudaStream_t stream) {

@@ -158,8 +158,9 @@ __device__ __forceinline__ float4 t5_ld_dsmem4(uint32_t local, uint32_t rank) {
 }
 
 // Partial tiles of a split: [row][NB + 4] floats (rows 16-byte aligned).
+__host__ __device__ constexpr int t5_part_stride_rt(int NB) { return NB + 4; }
 template <int NB>
-__host__ __device__ constexpr int t5_part_stride() { return NB + 4; }
+__host__ __device__ constexpr int t5_part_stride() { return t5_part_stride_rt(NB); }
 
 __device__ __forceinline__ uint64_t t5_policy_evict_last() {
   uint64_t p;
@@ -603,8 +604,49 @@ static bool t5_encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int es, const v
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch geometry of one GEMV on this kernel; host only, no device call.  False for shapes the
+// kernel does not take.
+bool plan_tc5(int M, int N, int K, int bs, int sms, Tc5Plan* o) {
+  // block sizes 32 ... 256 (each thread's 16-k slice lies in one block); K whole 64-k stages
+  if (M < 1 || M > 128 || N < 1 || K < kT5Kc || K % kT5Kc != 0 || bs < 32 || sms < 1) return false;
+  const int NB = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  // rings: 4 packed slots (64 KB of weights in flight per SM) and up to 8 stages (the A stages fill
+  // the rest of tensor memory), as many as fit in 227 KB with the 1 KB alignment slack
+  constexpr int NP = 4;
+  static_assert(NP <= kT5Sw, "one scale warp per packed slot");
+  int NS = 0;
+  for (int ns = kT5MaxStages; ns >= 4 && NS == 0; --ns) {
+    if (t5_layout(NB, NP, ns).total + 1024 <= 227 * 1024) NS = ns;
+  }
+  if (NS == 0) return false;
+  const T5Layout L = t5_layout(NB, NP, NS);
+  const int nrb = (N + kT5Rows - 1) / kT5Rows;
+  const int nchunk = K / kT5Kc;
+  const int nsc = (K + kT5Sk - 1) / kT5Sk;
+  // split K over a cluster when the row tiles fill fewer than half the SMs: enough CTAs to cover
+  // the SMs, at most 8 (a portable cluster) and at least one super-chunk each, and only when the
+  // stages saved outweigh the split's cost.  Measured on GB300: a 64-k stage costs about 0.37 us;
+  // a split costs about 3 us (cluster launch and barriers) plus 0.05 us per batch row (each CTA
+  // reads 32 M float4s through distributed shared memory, whatever ks).  The partial tile must
+  // fit in the x stages.
+  int ks = 1;
+  if (2 * nrb <= sms) {
+    ks = min(8, min(sms / nrb, nsc));
+    const double saved_us = 0.37 * nchunk * (1.0 - 1.0 / (ks > 0 ? ks : 1));
+    if (ks < 2 || saved_us < 0.05 * M + 3.0 || NS * L.xstage < kT5Rows * t5_part_stride_rt(NB) * 4) ks = 1;
+  }
+  o->nb = NB;
+  o->np = NP;
+  o->ns = NS;
+  o->ks = ks;
+  o->grid = ks > 1 ? nrb * ks : min(nrb, sms);
+  o->threads = kT5Threads;
+  o->smem = L.total + 1024;
+  return true;
+}
+
 template <int FMT, int NB>
-static cudaError_t launch_tc5_nb(T5Params& p, bool pdl, cudaStream_t stream) {
+static cudaError_t launch_tc5_nb(T5Params& p, const Tc5Plan& pl, bool pdl, cudaStream_t stream) {
   auto kern = w4_tc5_kernel<FMT, NB>;
   static bool attr_done = false;
   if (!attr_done) {
@@ -614,48 +656,23 @@ static cudaError_t launch_tc5_nb(T5Params& p, bool pdl, cudaStream_t stream) {
   }
   if (!t5_encode_2d(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.tm_x_base, p.K, p.M, kT5Kc, NB))
     return cudaErrorNotSupported;
-  // rings: 4 packed slots (64 KB of weights in flight per SM) and up to 8 stages (the A stages fill
-  // the rest of tensor memory), as many as fit in 227 KB with the 1 KB alignment slack
-  constexpr int NP = 4;
-  static_assert(NP <= kT5Sw, "one scale warp per packed slot");
-  int NS = 0;
-  for (int ns = kT5MaxStages; ns >= 4 && NS == 0; --ns) {
-    if (t5_layout(NB, NP, ns).total + 1024 <= 227 * 1024) NS = ns;
-  }
-  if (NS == 0) return cudaErrorNotSupported;
-  const T5Layout L = t5_layout(NB, NP, NS);
-  p.np = NP;
-  p.stages = NS;
-  const int nrb = (p.N + kT5Rows - 1) / kT5Rows;
-  const int sms = device_sm_count();
-  // split K over a cluster when the row tiles fill fewer than half the SMs: enough CTAs to cover
-  // the SMs, at most 8 (a portable cluster) and at least one super-chunk each, and only when the
-  // stages saved outweigh the split's cost.  Measured on GB300: a 64-k stage costs about 0.37 us;
-  // a split costs about 3 us (cluster launch and barriers) plus 0.05 us per batch row (each CTA
-  // reads 32 M float4s through distributed shared memory, whatever ks).  The partial tile must
-  // fit in the x stages.
-  int ks = 1;
-  if (2 * nrb <= sms) {
-    ks = min(8, min(sms / nrb, p.nsc));
-    const double saved_us = 0.37 * p.nchunk * (1.0 - 1.0 / (ks > 0 ? ks : 1));
-    if (ks < 2 || saved_us < 0.05 * p.M + 3.0 || NS * L.xstage < kT5Rows * t5_part_stride<NB>() * 4) ks = 1;
-  }
-  p.ks = ks;
-  const int grid = ks > 1 ? nrb * ks : min(nrb, sms);
+  p.np = pl.np;
+  p.stages = pl.ns;
+  p.ks = pl.ks;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kT5Threads);
-  cfg.dynamicSmemBytes = (size_t)L.total + 1024;
+  cfg.gridDim = dim3((unsigned)pl.grid);
+  cfg.blockDim = dim3((unsigned)pl.threads);
+  cfg.dynamicSmemBytes = (size_t)pl.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = (unsigned)ks;
+  attr[1].val.clusterDim.x = (unsigned)pl.ks;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = ks > 1 ? 2 : 1;
+  cfg.numAttrs = pl.ks > 1 ? 2 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   note_launch();
   return e;
@@ -664,9 +681,9 @@ static cudaError_t launch_tc5_nb(T5Params& p, bool pdl, cudaStream_t stream) {
 cudaError_t launch_gemv_tc5(int format, const uint8_t* packed, const void* scales, const float* codebook,
                             const __half* x, __half* y, int M, int N, int K, int bs, bool pdl,
                             cudaStream_t stream) {
-  // block sizes 32 ... 256 (each thread's 16-k slice lies in one block); the TMA copies need
-  // 16-byte aligned bases and rows
-  if (M < 1 || M > 128 || K % kT5Kc != 0 || bs < 32 || (reinterpret_cast<uintptr_t>(packed) & 15) ||
+  Tc5Plan pl;
+  // the TMA copies need 16-byte aligned bases
+  if (!plan_tc5(M, N, K, bs, device_sm_count(), &pl) || (reinterpret_cast<uintptr_t>(packed) & 15) ||
       (reinterpret_cast<uintptr_t>(x) & 15))
     return cudaErrorNotSupported;
   T5Params p;
@@ -678,16 +695,17 @@ cudaError_t launch_gemv_tc5(int format, const uint8_t* packed, const void* scale
   p.nchunk = K / kT5Kc;
   p.nsc = (K + kT5Sk - 1) / kT5Sk;
   p.ks = 1;
-  if (format == 0) {
-    if (M <= 16) return launch_tc5_nb<0, 16>(p, pdl, stream);
-    if (M <= 32) return launch_tc5_nb<0, 32>(p, pdl, stream);
-    if (M <= 64) return launch_tc5_nb<0, 64>(p, pdl, stream);
-    return launch_tc5_nb<0, 128>(p, pdl, stream);
+  switch (format * 1000 + pl.nb) {
+    case 16: return launch_tc5_nb<0, 16>(p, pl, pdl, stream);
+    case 32: return launch_tc5_nb<0, 32>(p, pl, pdl, stream);
+    case 64: return launch_tc5_nb<0, 64>(p, pl, pdl, stream);
+    case 128: return launch_tc5_nb<0, 128>(p, pl, pdl, stream);
+    case 1016: return launch_tc5_nb<1, 16>(p, pl, pdl, stream);
+    case 1032: return launch_tc5_nb<1, 32>(p, pl, pdl, stream);
+    case 1064: return launch_tc5_nb<1, 64>(p, pl, pdl, stream);
+    case 1128: return launch_tc5_nb<1, 128>(p, pl, pdl, stream);
+    default: return cudaErrorNotSupported;
   }
-  if (M <= 16) return launch_tc5_nb<1, 16>(p, pdl, stream);
-  if (M <= 32) return launch_tc5_nb<1, 32>(p, pdl, stream);
-  if (M <= 64) return launch_tc5_nb<1, 64>(p, pdl, stream);
-  return launch_tc5_nb<1, 128>(p, pdl, stream);
 }
 
 }  // namespace w4
