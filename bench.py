@@ -180,6 +180,45 @@ def oracle_sample_rate(budget_s: float, fmt: str = "nf4"):
     return done / dt / 1e9, cores, desc
 
 
+def cpu_practical_rate(budget_s: float):
+    """A practical CPU path beside the oracle (not the oracle, and not reachable from the library):
+    FP32 NumPy, nibbles unpacked and decoded per weight (code-book lookup times block absmax),
+    one BLAS matrix-vector product per GEMV on all cores, over the same row sample as the oracle
+    baseline, for about budget_s seconds.  Returns (GB/s of algorithmic bytes, cores, description)."""
+    import numpy as np
+    import oracle
+    from weight_only_bit_gb300 import synth
+    bs = 64
+    code64 = oracle.nf4_codebook()
+    code = np.asarray(code64, dtype=np.float32)
+    pool = []
+    for proj in ("q", "k", "v", "o", "gate", "up", "down"):
+        n, k = synth.shape_of(proj)
+        rows = min(n, 512)
+        w = synth.weights(synth.weight_seed(0, proj), n, k)[:rows]
+        x = synth.activations(synth.x_seed(0, synth.X_SLOT[proj], 1), 1, k)
+        p, s = oracle.quantize_nf4(w, code64, bs)
+        nbytes = rows * k // 2 + rows * (k // bs) * 4 + 2 * k + 2 * rows
+        pool.append((p, np.asarray(s, dtype=np.float32), x.astype(np.float32).reshape(-1), nbytes))
+    t0 = time.perf_counter()
+    done = 0
+    i = 0
+    while time.perf_counter() - t0 < budget_s:
+        p, s, x, nb = pool[i % len(pool)]
+        codes = np.empty((p.shape[0], 2 * p.shape[1]), dtype=np.uint8)
+        codes[:, 0::2] = p >> 4
+        codes[:, 1::2] = p & 15
+        w = code[codes] * np.repeat(s, bs, axis=1)
+        (w @ x).astype(np.float16)
+        done += nb
+        i += 1
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    desc = (f"NumPy FP32 dequantise + BLAS sgemv over the first 512 rows of layer 0's seven projections, "
+            f"{i} GEMVs in {dt:.1f} s")
+    return done / dt / 1e9, cores, desc
+
+
 def run_reference(args):
     """The oracle timed as the reference arm: each step a bounded row sample of the workload."""
     import numpy as np
@@ -373,6 +412,19 @@ def run_ours(args):
     ms_max = float(t.item())
     value = nbytes * world / (ms_max * 1e-3) / 1e9
 
+    # distribution of single steps (each bracketed by its own events, back to back, after the
+    # timed region): p10 / median / p90
+    nlat = 200
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nlat)]
+    for a, b in evs:
+        a.record(stream)
+        step.launch(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    lat = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    step_us_pct = {"p10": round(lat[nlat // 10], 2), "p50": round(lat[nlat // 2], 2), "p90": round(lat[9 * nlat // 10], 2),
+                   "steps": nlat}
+
     # end to end through the public API with host buffers: H2D of every x, the step, D2H of every y
     x_pin = torch.from_numpy(step.x_host).pin_memory()
     y_pin = torch.empty(step.y_elems, dtype=torch.float16).pin_memory()
@@ -430,12 +482,32 @@ def run_ours(args):
         shapes, weighted = per_shape("nf4", dev, torch, hbm)
         extra["per_shape_nf4"] = shapes
         extra["weighted_step_us_nf4"] = round(weighted, 2)
+        # read-only streaming ceiling: a library reduction reading a 2 GiB buffer once per pass
+        buf = torch.ones(1 << 29, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                torch.amax(buf)
+            r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            r0.record(stream)
+            for _ in range(10):
+                torch.amax(buf)
+            r1.record(stream)
+        torch.cuda.synchronize()
+        ro = 10 * buf.numel() * 4 / (r0.elapsed_time(r1) * 1e-3) / 1e9
+        extra["read_only_ceiling"] = {"GB_s": round(ro, 1), "frac_of_measured": round(ro / hbm, 4),
+                                      "kernel": "torch.amax over a 2 GiB FP32 buffer (library reduction, "
+                                                "every byte read once per pass)"}
+        del buf
+        torch.cuda.empty_cache()
     step.close()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs_cpu, cores, desc = oracle_sample_rate(float(os.environ.get("W4_CPU_BASELINE_S", "12")))
         cpu = {"value": round(gbs_cpu, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": desc}
+        gbs_p, cores_p, desc_p = cpu_practical_rate(float(os.environ.get("W4_CPU_PRACTICAL_S", "8")))
+        extra["cpu_practical"] = {"value": round(gbs_p, 4), "unit": "GB/s", "cores": cores_p,
+                                  "kind": "numpy FP32 dequantise-on-the-fly", "sample": desc_p}
 
     if rank == 0:
         achieved = nbytes / (ms_max * 1e-3) / 1e9     # one launch per step
@@ -454,6 +526,7 @@ def run_ours(args):
                          "peak_source": peak_src, "kernel": "w4_persistent_kernel<NF4,1> (the whole step)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
             "frac_of_nominal_8TBs": round(value / world / 8000.0, 4),
+            "step_us_percentiles": step_us_pct,
         }
         line.update(extra)
         print(json.dumps(line), flush=True)

@@ -67,7 +67,7 @@ typedef enum {
 typedef enum { W4_FMT_NF4 = 0, W4_FMT_INT4 = 1 } w4_format;
 
 /* Limits of this build. */
-#define W4_MAX_BATCH 128        /* M; prefill-sized GEMMs are not served                      */
+#define W4_MAX_BATCH 4096       /* M; above 128, batch tiles of 128 rows (prefill-sized)       */
 #define W4_MAX_K 10240          /* K; one consumer thread per 32-weight chunk of a row         */
 
 /* ---------------------------------------------------------------------------------------
@@ -119,7 +119,8 @@ int w4_dequantize_int4(const uint8_t* packed, const uint16_t* scale, float* W_ou
  * "Fused Kernel: Moving Dequantization On-Chip" and "Kernel Implementation"; FP32
  * accumulation as that kernel's comment requires).  y is rounded to FP16 (nearest even).
  * Batches 1 ... 8 run on CUDA cores; batches 9 ... 128 on the 5th-generation tensor cores
- * (tcgen05) when K is a multiple of 64, else on CUDA cores.
+ * (tcgen05) when K is a multiple of 64, else on CUDA cores.  Larger batches (prefill-sized,
+ * up to W4_MAX_BATCH) run as tiles of 128 batch rows, each tile one pass over the weights.
  * Sizes: 1 <= M <= W4_MAX_BATCH, N >= 1, 32 <= K <= W4_MAX_K, K % blocksize == 0,
  * blocksize a power of two in [32, 256].  packed, scales, x 16-byte aligned; y 2-byte aligned.
  * Agreement with the float64 definition: relative L2 error <= 1e-3 and
@@ -139,13 +140,14 @@ int w4_gemv_int4(const uint8_t* packed, const uint16_t* scale,
  * bitsandbytes (section "NF4: fast at batch 1, slower at larger batches").  Host only: no
  * device call, nothing allocated; *plan is caller-owned and fully written on W4_OK.
  *   kernel      W4_KERNEL_CUDA_CORES or W4_KERNEL_TCGEN05
- *   launches    kernel launches the call makes (CUDA cores: one per <= batch_tile rows)
+ *   launches    kernel launches the call makes (CUDA cores: one per <= batch_tile rows;
+ *               batches above 128: one set per 128-row batch tile)
  *   batch_tile  batch rows per launch (CUDA cores) or MMA N columns (tcgen05: 16/32/64/128)
  *   threads     threads per CTA; smem_bytes: dynamic shared memory per CTA
  *   stages      ring stages (CUDA cores: packed tiles; tcgen05: x / A stages)
  *   grid        CTAs per launch (tcgen05), or 0 where the launch sizes it from occupancy
  *   cluster     CTAs per thread-block cluster splitting K (1: no split)
- * For the CUDA cores the figures are those of the widest launch.  The mma.sync tensor-core
+ * The figures are those of the widest launch.  The mma.sync tensor-core
  * kernel, which serves only if the driver cannot encode TMA descriptors, is not predicted.
  * Errors: W4_ERR_NULL (plan NULL), W4_ERR_UNSUPPORTED (format, M > W4_MAX_BATCH or a shape
  * no kernel takes), W4_ERR_SHAPE / W4_ERR_BLOCKSIZE as for the GEMV, W4_ERR_SHAPE for

@@ -53,7 +53,7 @@ def test_gemv_validation(libw4):
     assert g(*ok, 1, 256, 1568, 64, None) == _lib.W4_ERR_SHAPE                      # K % bs != 0
     assert g(*ok, 0, 256, 1536, 64, None) == _lib.W4_ERR_SHAPE                      # empty batch
     assert g(*ok, 1, 0, 1536, 64, None) == _lib.W4_ERR_SHAPE                        # empty output
-    assert g(*ok, 129, 256, 1536, 64, None) == _lib.W4_ERR_UNSUPPORTED              # beyond the batch limit
+    assert g(*ok, 4097, 256, 1536, 64, None) == _lib.W4_ERR_UNSUPPORTED             # beyond the batch limit
     assert g(*ok, 1, 256, _lib.W4_MAX_K + 64, 64, None) == _lib.W4_ERR_UNSUPPORTED  # beyond the K limit
     assert g(A + 8, A, A, A, A, 1, 256, 1536, 64, None) == _lib.W4_ERR_ALIGN          # packed
     assert g(A, A + 4, A, A, A, 1, 256, 1536, 64, None) == _lib.W4_ERR_ALIGN          # absmax
@@ -189,9 +189,21 @@ def test_plan_validation(libw4):
     assert libw4.w4_gemv_plan(0, 1, 16, 64, 64, SMS, None) == w4.W4_ERR_NULL
     assert libw4.w4_gemv_plan(2, 1, 16, 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED
     assert libw4.w4_gemv_plan(0, 0, 16, 64, 64, SMS, ref) == w4.W4_ERR_SHAPE
-    assert libw4.w4_gemv_plan(0, 129, 16, 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED
+    assert libw4.w4_gemv_plan(0, 4097, 16, 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED
     assert libw4.w4_gemv_plan(0, 1, 0, 64, 64, SMS, ref) == w4.W4_ERR_SHAPE
     assert libw4.w4_gemv_plan(0, 1, 16, 96, 64, SMS, ref) == w4.W4_ERR_SHAPE
     assert libw4.w4_gemv_plan(0, 1, 16, 96, 48, SMS, ref) == w4.W4_ERR_BLOCKSIZE
     assert libw4.w4_gemv_plan(0, 1, 16, 64, 64, 0, ref) == w4.W4_ERR_SHAPE
     assert libw4.w4_gemv_plan(0, 1, 16, w4.W4_MAX_K + 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED
+
+
+def test_plan_prefill_batches_run_as_128_row_tiles(libw4):
+    nf4 = w4.W4_FMT_NF4
+    p = _plan(nf4, 300, *DECODE["gate"], 64)
+    assert p["kernel"] == w4.W4_KERNEL_TCGEN05 and p["batch_tile"] == 128 and p["launches"] == 3
+    assert _plan(nf4, 256, *DECODE["q"], 64)["launches"] == 2
+    assert _plan(nf4, 4096, *DECODE["q"], 64)["launches"] == 32
+    # a remainder of 8 rows or fewer goes to the CUDA cores: one more launch
+    assert _plan(nf4, 130, *DECODE["q"], 64)["launches"] == 2
+    # K not a multiple of 64: CUDA-core launches of 8 rows throughout
+    assert _plan(nf4, 300, 100, 96, 32)["launches"] == 38

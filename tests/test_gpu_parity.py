@@ -175,6 +175,8 @@ TC_CASES = [
     ("nf4", 16, 256, 1536, 64), ("int4", 16, 1000, 1600, 32), ("nf4", 24, 200, 320, 64), ("int4", 20, 8960, 1536, 128),
     ("nf4", 17, 128, 64, 64), ("int4", 24, 1536, 8960, 128), ("nf4", 40, 100, 96, 32), ("int4", 20, 100, 160, 32),
     ("int4", 128, 384, 768, 256), ("nf4", 64, 1536, 8960, 64), ("nf4", 9, 8960, 1536, 64), ("int4", 13, 300, 8960, 128),
+    # prefill-sized batches: 128-row batch tiles (a remainder of 2 rows on the CUDA cores)
+    ("nf4", 300, 640, 1536, 64), ("int4", 130, 257, 1024, 128),
     ("nf4", 32, 8960, 1536, 64), ("nf4", 32, 1536, 8960, 64), ("nf4", 33, 257, 1536, 64), ("nf4", 64, 129, 512, 32),
     ("nf4", 100, 300, 1536, 128), ("nf4", 128, 1536, 1536, 64), ("nf4", 128, 70, 8960, 256),
     ("int4", 32, 8960, 1536, 128), ("int4", 32, 1536, 8960, 128), ("int4", 47, 257, 1536, 64),

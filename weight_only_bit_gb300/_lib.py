@@ -26,7 +26,7 @@ W4_FMT_NF4 = 0
 W4_FMT_INT4 = 1
 W4_KERNEL_CUDA_CORES = 1
 W4_KERNEL_TCGEN05 = 2
-W4_MAX_BATCH = 128
+W4_MAX_BATCH = 4096
 W4_MAX_K = 10240
 
 # Every symbol include/w4.h declares.

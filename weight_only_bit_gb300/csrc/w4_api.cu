@@ -65,10 +65,23 @@ int check_gemv(int format, const uint8_t* packed, const void* scales, const floa
 // the CUDA cores, whose arithmetic the persistent step kernel shares bit for bit.
 bool tc5_batch(int M) { return M > 8; }
 
-// Enqueue one validated GEMV.  Batches above one CUDA-core launch's budget are split into
-// launches over consecutive batch rows (each re-reads the weights).
+// Largest batch one tensor-core launch takes; larger batches run as tiles of this many rows.
+constexpr int kBatchTile = 128;
+
+// Enqueue one validated GEMV.  Batches above one launch's budget are split into launches over
+// consecutive batch rows (each re-reads the weights): tiles of 128 rows, and within a tile the
+// CUDA-core launches of at most 8 rows where the tensor cores do not serve.
 int enqueue_gemv(int format, const uint8_t* packed, const void* scales, const float* codebook, const uint16_t* x,
                  uint16_t* y, int M, int N, int K, int bs, cudaStream_t stream) {
+  if (M > kBatchTile) {
+    for (int m0 = 0; m0 < M; m0 += kBatchTile) {
+      const int mm = (M - m0) < kBatchTile ? (M - m0) : kBatchTile;
+      const int s = enqueue_gemv(format, packed, scales, codebook, x + (size_t)m0 * K, y + (size_t)m0 * N, mm, N, K,
+                                 bs, stream);
+      if (s != W4_OK) return s;
+    }
+    return W4_OK;
+  }
   const __half* xh = reinterpret_cast<const __half*>(x);
   __half* yh = reinterpret_cast<__half*>(y);
   // batches above 8: the 5th-generation tensor cores (tcgen05; a batch below 16 is padded to 16
@@ -214,13 +227,8 @@ static int check_descs(const w4_gemv_desc* descs, int count) {
   return W4_OK;
 }
 
-int w4_gemv_plan(int format, int M, int N, int K, int blocksize, int sm_count, w4_gemv_plan_t* plan) {
-  if (!plan) return W4_ERR_NULL;
-  if (format != W4_FMT_NF4 && format != W4_FMT_INT4) return W4_ERR_UNSUPPORTED;
-  int s = check_shape(N, K, blocksize);
-  if (s != W4_OK) return s;
-  if (M < 1 || sm_count < 1) return W4_ERR_SHAPE;
-  if (M > W4_MAX_BATCH) return W4_ERR_UNSUPPORTED;
+// The plan of one batch tile (M <= kBatchTile), validated arguments.
+static int plan_tile(int format, int M, int N, int K, int blocksize, int sm_count, w4_gemv_plan_t* plan) {
   w4::Tc5Plan tp;
   if (tc5_batch(M) && w4::plan_tc5(M, N, K, blocksize, sm_count, &tp)) {
     *plan = w4_gemv_plan_t{W4_KERNEL_TCGEN05, 1, tp.nb, tp.threads, tp.smem, tp.ns, tp.grid, tp.ks};
@@ -229,6 +237,27 @@ int w4_gemv_plan(int format, int M, int N, int K, int blocksize, int sm_count, w
   w4::SimtPlan sp;
   if (!w4::plan_simt(format, M, K, blocksize, &sp)) return W4_ERR_UNSUPPORTED;
   *plan = w4_gemv_plan_t{W4_KERNEL_CUDA_CORES, sp.launches, sp.mb, sp.threads, sp.smem, sp.stages, 0, 1};
+  return W4_OK;
+}
+
+int w4_gemv_plan(int format, int M, int N, int K, int blocksize, int sm_count, w4_gemv_plan_t* plan) {
+  if (!plan) return W4_ERR_NULL;
+  if (format != W4_FMT_NF4 && format != W4_FMT_INT4) return W4_ERR_UNSUPPORTED;
+  int s = check_shape(N, K, blocksize);
+  if (s != W4_OK) return s;
+  if (M < 1 || sm_count < 1) return W4_ERR_SHAPE;
+  if (M > W4_MAX_BATCH) return W4_ERR_UNSUPPORTED;
+  if (M <= kBatchTile) return plan_tile(format, M, N, K, blocksize, sm_count, plan);
+  // full tiles of 128 rows, then the remainder tile; the figures are the full tile's
+  s = plan_tile(format, kBatchTile, N, K, blocksize, sm_count, plan);
+  if (s != W4_OK) return s;
+  plan->launches *= M / kBatchTile;
+  if (M % kBatchTile) {
+    w4_gemv_plan_t rest;
+    s = plan_tile(format, M % kBatchTile, N, K, blocksize, sm_count, &rest);
+    if (s != W4_OK) return s;
+    plan->launches += rest.launches;
+  }
   return W4_OK;
 }
 
