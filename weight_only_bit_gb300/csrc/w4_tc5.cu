@@ -108,7 +108,6 @@ __device__ __forceinline__ void t5_commit(uint64_t* bar) {
 
 __device__ __forceinline__ void t5_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void t5_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // 16 consecutive FP32 columns of this thread's tensor-memory lane.
 __device__ __forceinline__ void t5_ld16(uint32_t taddr, float (&v)[16]) {
