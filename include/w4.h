@@ -124,7 +124,9 @@ int w4_dequantize_int4(const uint8_t* packed, const uint16_t* scale, float* W_ou
  * Sizes: 1 <= M <= W4_MAX_BATCH, N >= 1, 32 <= K <= W4_MAX_K, K % blocksize == 0,
  * blocksize a power of two in [32, 256].  packed, scales, x 16-byte aligned; y 2-byte aligned.
  * Agreement with the float64 definition: relative L2 error <= 1e-3 and
- * max |error| <= 2e-2 * RMS(y) per output vector.
+ * max |error| <= 2e-2 * RMS(y) per output vector.  The tensor-core paths multiply in FP16, so
+ * for them an NF4 absmax must stay below 65504 (the FP16 range; the FP32 absmax is rounded
+ * to FP16) and so must every |x| and every decoded weight.
  */
 int w4_gemv_nf4(const uint8_t* packed, const float* absmax, const float* codebook,
                 const uint16_t* x, uint16_t* y, int M, int N, int K, int blocksize,
