@@ -234,10 +234,12 @@ int w4_device_check(w4_stream_t stream);
 /* Kernel launches the library has issued in this process (for launch accounting). */
 long long w4_launch_count(void);
 
-/* Test hook for the timeout path.  The next CUDA-core GEMV launch in this process has its
- * producer warp issue no copies, so every consumer's bounded wait (one second) runs out; the
- * kernel records the failure and returns without faulting, its output is garbage, and the next
- * w4_device_check() returns W4_ERR_TIMEOUT.  The context stays usable.  Returns W4_OK. */
+/* Test hook for the timeout path.  The next GEMV launch in this process (CUDA-core or tcgen05
+ * kernel, whichever the call dispatches to) has its weight producer issue no copies, so the bounded
+ * waits (one second each) of the roles that depend on those copies run out; the kernel records the
+ * failure, waits (bounded) for whatever copies and MMAs it did issue, frees its tensor memory and
+ * returns without faulting.  Its output is garbage, and the next w4_device_check() returns
+ * W4_ERR_TIMEOUT.  The context stays usable.  Returns W4_OK. */
 int w4_inject_timeout_once(void);
 
 #ifdef __cplusplus

@@ -302,3 +302,27 @@ def test_timeout_is_reported_and_context_survives(dev):
     assert w4.w4_device_check() == 0                      # cleared after reading
     y = gpu_gemv("nf4", packed, sc, x, n, k, bs, dev)
     assert_gemv_close(y.cpu().numpy(), oracle_gemv("nf4", p_ref, s_ref, x, bs))
+
+
+@pytest.mark.parametrize("n,k", [(1024, 1536), (8960, 1536)])
+def test_tensor_core_timeout_is_reported_and_context_survives(dev, n, k):
+    """The same host-set hook on the tcgen05 kernel (batch 32): its packed producer issues no
+    copies, so the decoders', scale warps', MMA issuer's and epilogue's bounded waits run out; the
+    kernel still waits for the x copies it issued, frees its tensor memory and returns.  The host
+    reads W4_ERR_TIMEOUT from the tensor-core kernel's own error word, and the next call matches
+    the oracle.  (1024 rows: split-K over a thread-block cluster; 8960 rows: no split.)"""
+    bs, m = 64, 32
+    st, plan = w4.w4_gemv_plan(w4._lib.W4_FMT_NF4, m, n, k, bs)
+    assert st == 0 and plan["kernel"] == w4.W4_KERNEL_TCGEN05
+    w = synth.weights(9100 + n, n, k)
+    x = synth.activations(9101 + n, m, k)
+    p_ref, s_ref = oracle_quantize("nf4", w, bs)
+    packed, sc = _t(p_ref, dev), _t(s_ref, dev)
+    assert w4.w4_device_check() == 0
+    w4.w4_inject_timeout_once()
+    gpu_gemv("nf4", packed, sc, x, n, k, bs, dev)
+    assert w4.w4_device_check() == w4._lib.W4_ERR_TIMEOUT
+    assert w4.w4_device_check() == 0
+    rows = np.unique(np.concatenate([[0, n - 1], np.random.default_rng(n).integers(0, n, 64)]))
+    y = gpu_gemv("nf4", packed, sc, x, n, k, bs, dev).cpu().numpy()
+    assert_gemv_close(y[:, rows], oracle_gemv("nf4", p_ref, s_ref, x, bs, rows=rows))

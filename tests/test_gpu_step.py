@@ -38,10 +38,11 @@ def _check_step(step, rows_per_gemv=8, seed=0):
         assert np.all(rel <= 1e-3), (layer, proj, rel)
 
 
-@pytest.mark.parametrize("levels", ["grouped", "strict"])
-def test_full_nf4_step_graph(dev, levels):
+@pytest.mark.parametrize("fmt,levels", [("nf4", "grouped"), ("nf4", "strict"), ("int4", "grouped")])
+def test_full_step_graph(dev, fmt, levels):
+    """The whole 197-GEMV step (113 levels grouped, 197 strict) in one persistent launch."""
     from weight_only_bit_gb300.step import DecodeStep
-    step = DecodeStep("nf4", batch=1, device=str(dev), levels=levels).build().capture()
+    step = DecodeStep(fmt, batch=1, device=str(dev), levels=levels).build().capture()
     assert len(step.gemvs) == 197
     assert step.levels[-1] == (112 if levels == "grouped" else 196)
     stream = torch.cuda.Stream(dev)

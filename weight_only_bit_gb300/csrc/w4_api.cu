@@ -21,8 +21,6 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 static std::atomic<int> g_inject{0};
 int take_fault_injection() { return g_inject.exchange(0); }
 
-unsigned int read_clear_error_gemv();
-
 }  // namespace w4
 
 namespace {
@@ -401,7 +399,8 @@ int w4_last_cuda_error(void) { return t_last_cuda_error; }
 int w4_device_check(w4_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_status(e);
-  unsigned int v = w4::read_clear_error_gemv();
+  // every translation unit's copy of the error word: the CUDA-core and the tensor-core kernels
+  const unsigned int v = w4::read_clear_error_persist() | w4::read_clear_error_tc5();
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);
   return v ? W4_ERR_TIMEOUT : W4_OK;

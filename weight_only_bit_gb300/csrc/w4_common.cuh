@@ -6,13 +6,25 @@
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 
 namespace w4 {
 
-// Set by a kernel whose bounded wait ran out (never by a normal run); read and cleared by
-// w4_device_check() through each translation unit's reader.  Values: 0 = fine, otherwise a site
-// code identifying the wait.  One word per translation unit (no relocatable device code).
+// Set by a kernel whose bounded wait ran out (never by a normal run).  Values: 0 = fine, otherwise
+// a site code identifying the wait.  Without relocatable device code every translation unit that
+// includes this header holds its own copy of the word, so each one whose kernels wait exports a
+// reader built on read_clear_error_word_here(), and w4_device_check() combines all of them.
 static __device__ unsigned int g_error_word = 0;
+
+// Host side: reads and clears this translation unit's copy of the error word on the current device
+// (synchronous with respect to the device).
+static inline unsigned int read_clear_error_word_here() {
+  unsigned int v = 0;
+  const unsigned int z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return 0;
+  if (v != 0) cudaMemcpyToSymbol(g_error_word, &z, sizeof(z));
+  return v;
+}
 
 // Wall-clock limit of one mbarrier wait.  A healthy wait ends within microseconds (one DRAM
 // round trip); a wait still open after a second is treated as lost.

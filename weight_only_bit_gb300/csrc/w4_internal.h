@@ -58,6 +58,11 @@ int simt_max_batch(int format, int K, int bs);
 
 int device_sm_count();
 
+// Each translation unit's device error word (see w4_common.cuh), read and cleared on the current
+// device: the CUDA-core kernels' and the tcgen05 kernel's.
+unsigned int read_clear_error_persist();
+unsigned int read_clear_error_tc5();
+
 // A whole decode step in one persistent CUDA-core launch.  GEMVs are grouped into levels (0, 1, ...
 // non-decreasing along the array); a level reads its x only after every GEMV of the previous level
 // is complete.  counters: caller-owned device memory of (number of levels + 1) words, zero before

@@ -770,11 +770,6 @@ cudaError_t launch_step_simt_noalloc(int format, const StepJob* jobs, int n, int
   return launch_step_simt(format, jobs, n, M, codebook, counters, true, stream);
 }
 
-unsigned int read_clear_error_gemv() {
-  unsigned int v = 0, z = 0;
-  cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v));
-  cudaMemcpyToSymbol(g_error_word, &z, sizeof(z));
-  return v;
-}
+unsigned int read_clear_error_persist() { return read_clear_error_word_here(); }
 
 }  // namespace w4

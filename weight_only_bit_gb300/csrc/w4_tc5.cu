@@ -70,6 +70,7 @@ struct T5Params {
   int nsc;           // super-chunks per tile
   int stages;        // x / A stages
   int np;            // packed slots
+  int inject_timeout;  // test hook: the packed producer issues no copies (every wait then runs out)
 };
 
 // Shared-memory matrix descriptor of B (version 1): 128-byte swizzle (layout type 2 in bits 61-63),
@@ -302,7 +303,7 @@ __global__ void __launch_bounds__(kT5Threads, 1) w4_tc5_kernel(const __grid_cons
 
   if (warp == kT5Pw) {
     // ================================================================ packed producer
-    if (lane == 0) {
+    if (lane == 0 && !p.inject_timeout) {
       const uint64_t pol = policy_evict_first();
       const uint32_t pk = smem_u32(smem + Lo.packed);
       auto prefetch_scales = [&](int rb) {
@@ -694,6 +695,7 @@ cudaError_t launch_gemv_tc5(int format, const uint8_t* packed, const void* scale
   p.nchunk = K / kT5Kc;
   p.nsc = (K + kT5Sk - 1) / kT5Sk;
   p.ks = 1;
+  p.inject_timeout = take_fault_injection();
   switch (format * 1000 + pl.nb) {
     case 16: return launch_tc5_nb<0, 16>(p, pl, pdl, stream);
     case 32: return launch_tc5_nb<0, 32>(p, pl, pdl, stream);
@@ -706,5 +708,7 @@ cudaError_t launch_gemv_tc5(int format, const uint8_t* packed, const void* scale
     default: return cudaErrorNotSupported;
   }
 }
+
+unsigned int read_clear_error_tc5() { return read_clear_error_word_here(); }
 
 }  // namespace w4
