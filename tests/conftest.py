@@ -8,6 +8,10 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built libw4")
+    # a per-test limit where the pytest-timeout plugin is installed (every device wait is bounded, so
+    # a test that runs this long is stuck in a chain of expiring waits, not computing)
+    if config.pluginmanager.hasplugin("timeout") and not getattr(config.option, "timeout", None):
+        config.option.timeout = 600
 
 
 import pytest

@@ -50,7 +50,7 @@ def test_full_step_graph(dev, fmt, levels):
     w4.check(step.launch(stream))
     torch.cuda.synchronize()
     assert w4.w4_launch_count() - l0 == 1                  # the whole step is one persistent launch
-    assert torch.all(step.workspace == 0)                  # counters left at zero for the next launch
+    assert torch.all(step.counters() == 0)                 # counters left at zero for the next launch
     assert w4.w4_device_check(stream) == 0
     g = step.y.clone()
     _check_step(step)
@@ -66,7 +66,7 @@ def test_full_step_graph(dev, fmt, levels):
     torch.cuda.synchronize()
     assert w4.w4_device_check(stream) == 0
     assert torch.equal(step.y.view(torch.int16), g.view(torch.int16))
-    assert torch.all(step.workspace == 0)
+    assert torch.all(step.counters() == 0)
     step.close()
 
 
@@ -83,6 +83,23 @@ def test_reduced_steps(dev, fmt, batch):
     step.close()
 
 
+@pytest.mark.parametrize("levels", ["strict", "grouped"])
+def test_one_layer_steps_replayed_back_to_back(dev, levels):
+    """A one-layer step replayed several times in a row: every level's first tile must reach the
+    ring even while the stream gate is closed (the consumers wait for it before they wait for the
+    previous level), so no bounded wait may run out."""
+    from weight_only_bit_gb300.step import DecodeStep
+    step = DecodeStep("nf4", batch=1, device=str(dev), layers=1, lm_head=False, levels=levels).build().capture()
+    stream = torch.cuda.Stream(dev)
+    for _ in range(4):
+        w4.check(step.launch(stream))
+    torch.cuda.synchronize()
+    assert w4.w4_device_check(stream) == 0
+    assert torch.all(step.counters() == 0)
+    _check_step(step, rows_per_gemv=16, seed=3)
+    step.close()
+
+
 def test_step_timeout_path_recovers(dev):
     """The injected producer failure inside a multi-level persistent step: every bounded wait ends,
     the host reads W4_ERR_TIMEOUT, the counters are left at zero and the next replay is right."""
@@ -95,7 +112,7 @@ def test_step_timeout_path_recovers(dev):
     w4.check(step.launch(stream))
     torch.cuda.synchronize()
     assert w4.w4_device_check(stream) == w4._lib.W4_ERR_TIMEOUT
-    assert torch.all(step.workspace == 0)
+    assert torch.all(step.counters() == 0)
     step.close()
     step.capture()
     w4.check(step.launch(stream))
@@ -177,5 +194,5 @@ def test_chained_levels_read_previous_outputs(dev, fmt, batch):
     assert w4.w4_device_check(stream) == 0
     for a, b in zip(got, ys):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    assert torch.all(workspace == 0)
+    assert torch.all(workspace[: len(descs) + 1] == 0)          # the level counters
     w4.check(w4.w4_step_destroy(h))

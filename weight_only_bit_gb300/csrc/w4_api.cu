@@ -271,9 +271,18 @@ int w4_gemv_sequence(const w4_gemv_desc* descs, int count, w4_stream_t stream) {
   return W4_OK;
 }
 
+// Step workspace: (count + 1) level counters, then, 64-byte aligned, one 128-byte TMA tensor map per
+// descriptor (written once by w4_step_create, read by every launch).
+static size_t ws_counter_bytes(int count) { return ((size_t)(count + 1) * 4 + 15) & ~(size_t)15; }
+
+static CUtensorMap* ws_maps(void* workspace, int count) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(workspace) + ws_counter_bytes(count);
+  return reinterpret_cast<CUtensorMap*>((a + 63) & ~(uintptr_t)63);
+}
+
 int64_t w4_step_workspace_bytes(int count) {
   if (count < 1) return 0;
-  return ((int64_t)(count + 1) * 4 + 255) / 256 * 256;
+  return ((int64_t)ws_counter_bytes(count) + 64 + (int64_t)count * (int64_t)sizeof(CUtensorMap) + 255) / 256 * 256;
 }
 
 // True when the step can run as one persistent CUDA-core launch.
@@ -299,8 +308,25 @@ int w4_step_create(const w4_gemv_desc* descs, int count, void* workspace, w4_ste
   cudaStream_t cs = nullptr;
   cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
   if (e != cudaSuccess) return cuda_status(e);
+  std::vector<w4::StepJob> jobs;
   if (persistent) {
-    e = cudaMemsetAsync(workspace, 0, (size_t)w4_step_workspace_bytes(count), cs);
+    jobs.resize((size_t)count);
+    for (int i = 0; i < count; ++i) {
+      const w4_gemv_desc& d = descs[i];
+      jobs[i] = w4::StepJob{d.packed, d.scales, reinterpret_cast<const __half*>(d.x), reinterpret_cast<__half*>(d.y),
+                            d.N, d.K, d.blocksize, d.level};
+    }
+    // counters zeroed, tensor maps written once, before the capture
+    std::vector<CUtensorMap> maps((size_t)count);
+    e = w4::step_simt_maps(descs[0].format, jobs.data(), count, descs[0].M, maps.data());
+    if (e == cudaErrorNotSupported) {
+      cudaStreamDestroy(cs);
+      return W4_ERR_UNSUPPORTED;
+    }
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, (size_t)w4_step_workspace_bytes(count), cs);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ws_maps(workspace, count), maps.data(), sizeof(CUtensorMap) * (size_t)count,
+                          cudaMemcpyHostToDevice, cs);
     if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
     if (e != cudaSuccess) {
       cudaStreamDestroy(cs);
@@ -312,14 +338,8 @@ int w4_step_create(const w4_gemv_desc* descs, int count, void* workspace, w4_ste
   e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   if (e == cudaSuccess) {
     if (persistent) {
-      std::vector<w4::StepJob> jobs((size_t)count);
-      for (int i = 0; i < count; ++i) {
-        const w4_gemv_desc& d = descs[i];
-        jobs[i] = w4::StepJob{d.packed, d.scales, reinterpret_cast<const __half*>(d.x), reinterpret_cast<__half*>(d.y),
-                              d.N, d.K, d.blocksize, d.level};
-      }
       cudaError_t e3 = w4::launch_step_simt(descs[0].format, jobs.data(), count, descs[0].M, descs[0].codebook,
-                                            reinterpret_cast<unsigned*>(workspace), true, cs);
+                                            reinterpret_cast<unsigned*>(workspace), ws_maps(workspace, count), true, cs);
       if (e3 != cudaSuccess) s = (e3 == cudaErrorNotSupported) ? W4_ERR_UNSUPPORTED : cuda_status(e3);
     } else {
       for (int i = 0; i < count && s == W4_OK; ++i) {

@@ -1,6 +1,7 @@
 // w4_internal.h -- host-side declarations shared by libw4's translation units (not installed).
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -58,15 +59,22 @@ int simt_max_batch(int format, int K, int bs);
 
 int device_sm_count();
 
+// 2-D tiled TMA map over a row-major [rows][cols] array of 1-byte (es = 1) or FP16 (es = 2) elements:
+// box of box_cols x box_rows, 128-byte swizzle, zeros outside the array.  False if the driver
+// cannot encode it (base not 16-byte aligned, row bytes not a multiple of 16, ...).
+bool encode_tmap_2d(CUtensorMap* m, int es, const void* base, long long cols, long long rows, int box_cols,
+                    int box_rows);
+
 // Each translation unit's device error word (see w4_common.cuh), read and cleared on the current
 // device: the CUDA-core kernels' and the tcgen05 kernel's.
 unsigned int read_clear_error_persist();
 unsigned int read_clear_error_tc5();
 
-// A whole decode step in one persistent CUDA-core launch.  GEMVs are grouped into levels (0, 1, ...
-// non-decreasing along the array); a level reads its x only after every GEMV of the previous level
-// is complete.  counters: caller-owned device memory of (number of levels + 1) words, zero before
-// the first launch; the kernel leaves it zero again.
+// A whole decode step in one persistent launch of the batch 1 ... 8 kernel.  GEMVs are grouped into
+// levels (0, 1, ... non-decreasing along the array); a level reads its x only after every GEMV of
+// the previous level is complete.  counters: device memory of (number of levels + 1) words, zero
+// before the first launch; the kernel leaves it zero again.  maps: device memory holding the n
+// tensor maps step_simt_maps() returns for the same arguments (64-byte aligned, 128 bytes each).
 constexpr int kStepMaxGemvs = 256;
 struct StepJob {
   const uint8_t* packed;
@@ -75,10 +83,12 @@ struct StepJob {
   __half* y;
   int N, K, bs, level;
 };
+cudaError_t step_simt_maps(int format, const StepJob* jobs, int n, int M, CUtensorMap* maps_out);
 cudaError_t launch_step_simt(int format, const StepJob* jobs, int n, int M, const float* codebook, unsigned* counters,
-                             bool pdl, cudaStream_t stream);
+                             const CUtensorMap* maps, bool pdl, cudaStream_t stream);
 
-// The same launch with the level counters in a fixed array inside the library (no caller memory).
+// The same launch with the level counters and the tensor maps in fixed arrays inside the library (no
+// caller memory): the maps are copied in on `stream` before the launch.
 int noalloc_max_levels();
 cudaError_t launch_step_simt_noalloc(int format, const StepJob* jobs, int n, int M, const float* codebook,
                                      int nlevels, cudaStream_t stream);

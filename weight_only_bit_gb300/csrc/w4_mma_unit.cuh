@@ -1,0 +1,304 @@
+// w4_mma_unit.cuh -- the decode-and-multiply unit of the batch 1 ... 8 kernel: 16 weight rows x 256 k
+// of a tile in shared memory, decoded through the byte-pair table into mma.sync.m16n8k16 A fragments
+// (FP16 x FP16 -> FP32) against x, with the block scales applied to FP32 accumulators.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "w4_common.cuh"
+#include "w4_decode.cuh"
+
+namespace w4 {
+
+constexpr int kSpanK = 128;            // k per unit of work (one partial sum per row and span)
+constexpr int kBoxK = 256;             // k per TMA box (128 bytes of a row): two spans
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Shared-memory loads by 32-bit shared address.  The table loads are plain asm: the table is
+// constant once built, and each address depends on packed data loaded after the stage's wait.  The
+// ring loads are volatile, so they stay after the wait that makes their data valid.
+__device__ __forceinline__ uint32_t lds_table(uint32_t a) {
+  uint32_t v;
+  asm("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_ring32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_ring64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_scale32(uint32_t a) { return __uint_as_float(lds_ring32(a)); }
+__device__ __forceinline__ float lds_scale16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return __half2float(__ushort_as_half(v));
+}
+
+// Decoded pair (element 2j in the low half) of packed byte b (0 ... 3) of word w, from this lane's
+// copy of the byte-pair table (lut_lane: shared address of the lane's entry 0).
+__device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lane, uint32_t w, int b) {
+  uint32_t byte;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(byte) : "r"(w), "r"(0x4440 + b));
+  return lds_table(lut_lane + (byte << 7));
+}
+
+// Byte-pair table for the format: entry b = half2(v(b >> 4), v(b & 15)), one copy per lane (entry b
+// of lane l at word 32 b + l, so any pattern of bytes across a warp is conflict-free).
+//   NF4: v(q) = fp16(code[q]);  INT4: v(q) = q - 8;  FP4 (E2M1, sign in bit 3): v(q) = +-{0, 0.5, 1,
+//   1.5, 2, 3, 4, 6}[q & 7] ("LLM Compressor 0.14", section "Details worth knowing": the E2M1 grid).
+__device__ __forceinline__ float nibble_value(int fmt, const float* __restrict__ codebook, int q) {
+  if (fmt == 0) return __ldg(codebook + q);
+  if (fmt == 1) return (float)(q - 8);
+  const int mag = q & 7;
+  const float v = mag < 4 ? 0.5f * (float)mag : (float)(1 << (mag - 2)) * (mag & 1 ? 1.5f : 1.0f);
+  return (q & 8) ? -v : v;
+}
+
+__device__ __forceinline__ void build_lut(uint32_t* lut, int fmt, const float* __restrict__ codebook, int t,
+                                          int nthreads) {
+  for (int i = t; i < 256 * 32; i += nthreads) {
+    const int b = i >> 5;
+    const __half lo = __float2half_rn(nibble_value(fmt, codebook, b >> 4));
+    const __half hi = __float2half_rn(nibble_value(fmt, codebook, b & 15));
+    lut[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+  }
+}
+
+// Sum of one output's partials rr[0 .. C) in order (16-byte loads; rr 16-byte aligned).
+__device__ __forceinline__ float sum_spans(const float* rr, int C) {
+  float s = 0.0f;
+  int c = 0;
+  for (; c + 4 <= C; c += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(rr + c);
+    s += v.x;
+    s += v.y;
+    s += v.z;
+    s += v.w;
+  }
+  for (; c < C; ++c) s += rr[c];
+  return s;
+}
+
+// Loads the NSC = max(1, 128 / bs) scales of one span of one row (NSC * ES bytes, aligned to that
+// size when K is a multiple of 128) and expands them to one FP32 scale per k block.
+template <int KB, bool SC32, int NSC>
+__device__ __forceinline__ void span_scales(float (&sk)[kSpanK / KB], uint32_t a) {
+  constexpr int NKB = kSpanK / KB;
+  constexpr int ES = SC32 ? 4 : 2;
+  constexpr int BYTES = NSC * ES;
+  uint32_t w[8];
+  if (BYTES >= 16) {
+#pragma unroll
+    for (int q = 0; q < BYTES / 16; ++q) {
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(w[4 * q]), "=r"(w[4 * q + 1]), "=r"(w[4 * q + 2]), "=r"(w[4 * q + 3]) : "r"(a + 16 * q));
+    }
+  } else if (BYTES == 8) {
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(a));
+  } else if (BYTES == 4) {
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[0]) : "r"(a));
+  } else {
+    unsigned short h;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+    w[0] = h;
+  }
+  float v[NSC];
+#pragma unroll
+  for (int i = 0; i < NSC; ++i) {
+    if (SC32) {
+      v[i] = __uint_as_float(w[i]);
+    } else {
+      const uint32_t word = w[i >> 1];
+      v[i] = __half2float(__ushort_as_half((unsigned short)((i & 1) ? (word >> 16) : (word & 0xffffu))));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NKB; ++j) sk[j] = v[j / (NKB / NSC)];
+}
+
+// One unit: 16 weight rows x one span (128 k) of a tile.  a0, a1: shared addresses of the span's
+// row of MMA row g and of MMA row g + 8 (128 bytes each); off0[j], off1[j]: this lane's byte offset
+// of k block j in those swizzled rows; s0a, s1a: their scale rows (at the span's first scale); v0 /
+// v1 false for rows beyond the tile (their scales are zeroed); xg: this lane's x elements of the
+// span, loaded only where xok (batch row g exists; columns at or above the batch are never
+// stored).  NSC > 0: the span is full and its NSC scales per row are one aligned vector (K a
+// multiple of 128); NSC == 0: the general case, nkb k blocks present, scale index of block j =
+// sidx0 + (j >> sshift) relative to s0a / s1a.
+// KB = 64: per 64-k block, 8 packed bytes per lane per row and 4 MMAs; KB = 32: 4 bytes, 2 MMAs.
+// acc[0], acc[1]: MMA row g, batch rows 2t, 2t + 1; acc[2], acc[3]: MMA row g + 8.
+template <int KB, bool SC32, int NSC>
+__device__ __forceinline__ void mma_unit(float (&acc)[4], uint32_t a0, uint32_t a1, const uint32_t (&off0)[kSpanK / KB],
+                                         const uint32_t (&off1)[kSpanK / KB], uint32_t s0a, uint32_t s1a,
+                                         bool v0, bool v1, const uint8_t* xg, bool xok, int sidx0, int sshift, int nkb,
+                                         uint32_t lut_lane, int lane) {
+  constexpr int NKB = kSpanK / KB;     // k blocks per full span
+  constexpr int RUN = KB / 8;          // packed bytes per lane per row per k block
+  constexpr int NMMA = KB / 16;        // MMAs per k block
+  constexpr bool FULL = NSC > 0;
+  constexpr int ES = SC32 ? 4 : 2;
+  const int t = lane & 3;
+  // x of this lane's batch row: KB/4 halves (KB/2 bytes) per k block
+  uint32_t xr[NKB][KB / 8];
+#pragma unroll
+  for (int j = 0; j < NKB; ++j) {
+#pragma unroll
+    for (int q = 0; q < KB / 32; ++q) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (xok && (FULL || j < nkb)) v = ld_x_v4(xg + j * (KB * 2) + 16 * q);
+      xr[j][4 * q + 0] = v.x; xr[j][4 * q + 1] = v.y; xr[j][4 * q + 2] = v.z; xr[j][4 * q + 3] = v.w;
+    }
+  }
+  // packed bytes of both rows, per k block
+  uint32_t w0[NKB][RUN / 4], w1[NKB][RUN / 4];
+#pragma unroll
+  for (int j = 0; j < NKB; ++j) {
+    if (FULL || j < nkb) {
+      if (RUN == 8) {
+        const uint2 p = lds_ring64(a0 + off0[j]), q = lds_ring64(a1 + off1[j]);
+        w0[j][0] = p.x; w0[j][RUN / 4 - 1] = p.y;
+        w1[j][0] = q.x; w1[j][RUN / 4 - 1] = q.y;
+      } else {
+        w0[j][0] = lds_ring32(a0 + off0[j]);
+        w1[j][0] = lds_ring32(a1 + off1[j]);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < RUN / 4; ++i) w0[j][i] = w1[j][i] = 0u;
+    }
+  }
+  // one scale per k block and row
+  float sk0[NKB], sk1[NKB];
+  if (FULL) {
+    span_scales<KB, SC32, (NSC > 0 ? NSC : 1)>(sk0, s0a);
+    span_scales<KB, SC32, (NSC > 0 ? NSC : 1)>(sk1, s1a);
+  } else {
+    // lane t loads blocks j = t, t + 4 for both rows; shuffled per block
+    constexpr int NH = (NKB + 3) / 4;
+    float sv0[NH], sv1[NH];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) {
+      const int j = t + 4 * h;
+      float a = 0.0f, b = 0.0f;
+      if (j < nkb) {
+        const uint32_t off = (uint32_t)((sidx0 + (j >> sshift)) * ES);
+        a = SC32 ? lds_scale32(s0a + off) : lds_scale16(s0a + off);
+        b = SC32 ? lds_scale32(s1a + off) : lds_scale16(s1a + off);
+      }
+      sv0[h] = a;
+      sv1[h] = b;
+    }
+#pragma unroll
+    for (int j = 0; j < NKB; ++j) {
+      sk0[j] = __shfl_sync(0xffffffffu, sv0[j / 4], (lane & ~3) | (j & 3));
+      sk1[j] = __shfl_sync(0xffffffffu, sv1[j / 4], (lane & ~3) | (j & 3));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NKB; ++j) {
+    if (!v0) sk0[j] = 0.0f;
+    if (!v1) sk1[j] = 0.0f;
+  }
+#pragma unroll
+  for (int j = 0; j < NKB; ++j) {
+    if (FULL || j < nkb) {
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int s = 0; s < NMMA; ++s) {
+        // slot t: packed byte 2s of the lane's run (k 4s, 4s + 1); slot t + 4: byte 2s + 1
+        const uint32_t ww0 = w0[j][(2 * s) >> 2], ww1 = w1[j][(2 * s) >> 2];
+        const int b = (2 * s) & 3;
+        const uint32_t a[4] = {lut_pair(lut_lane, ww0, b), lut_pair(lut_lane, ww1, b), lut_pair(lut_lane, ww0, b + 1),
+                               lut_pair(lut_lane, ww1, b + 1)};
+        mma16816(d, a, xr[j][2 * s], xr[j][2 * s + 1]);
+      }
+      acc[0] = fmaf(sk0[j], d[0], acc[0]);
+      acc[1] = fmaf(sk0[j], d[1], acc[1]);
+      acc[2] = fmaf(sk1[j], d[2], acc[2]);
+      acc[3] = fmaf(sk1[j], d[3], acc[3]);
+    }
+  }
+}
+
+// The same unit split in two, so that the weights of a unit can be decoded before its x exists:
+// decode_unit turns the packed bytes of both rows into the A fragments of every MMA of the span and
+// loads the scales (FULL spans, NSC scales per row as one vector); mma_decoded loads x and runs the
+// MMAs.  Together they compute what mma_unit<KB, SC32, NSC> computes, in the same order.
+template <int KB>
+struct DecodedUnit {
+  uint32_t a[kSpanK / KB][KB / 16][4];
+  float sk0[kSpanK / KB], sk1[kSpanK / KB];
+};
+
+template <int KB, bool SC32, int NSC>
+__device__ __forceinline__ void decode_unit(DecodedUnit<KB>& du, uint32_t a0, uint32_t a1,
+                                            const uint32_t (&off0)[kSpanK / KB], const uint32_t (&off1)[kSpanK / KB],
+                                            uint32_t s0a, uint32_t s1a, bool v0, bool v1, uint32_t lut_lane) {
+  constexpr int NKB = kSpanK / KB;
+  constexpr int NMMA = KB / 16;
+#pragma unroll
+  for (int j = 0; j < NKB; ++j) {
+    uint32_t w0[2], w1[2];
+    if (KB == 64) {
+      const uint2 p = lds_ring64(a0 + off0[j]), q = lds_ring64(a1 + off1[j]);
+      w0[0] = p.x; w0[1] = p.y; w1[0] = q.x; w1[1] = q.y;
+    } else {
+      w0[0] = w0[1] = lds_ring32(a0 + off0[j]);
+      w1[0] = w1[1] = lds_ring32(a1 + off1[j]);
+    }
+#pragma unroll
+    for (int s = 0; s < NMMA; ++s) {
+      const uint32_t ww0 = w0[(2 * s) >> 2], ww1 = w1[(2 * s) >> 2];
+      const int b = (2 * s) & 3;
+      du.a[j][s][0] = lut_pair(lut_lane, ww0, b);
+      du.a[j][s][1] = lut_pair(lut_lane, ww1, b);
+      du.a[j][s][2] = lut_pair(lut_lane, ww0, b + 1);
+      du.a[j][s][3] = lut_pair(lut_lane, ww1, b + 1);
+    }
+  }
+  span_scales<KB, SC32, NSC>(du.sk0, s0a);
+  span_scales<KB, SC32, NSC>(du.sk1, s1a);
+#pragma unroll
+  for (int j = 0; j < NKB; ++j) {
+    if (!v0) du.sk0[j] = 0.0f;
+    if (!v1) du.sk1[j] = 0.0f;
+  }
+}
+
+template <int KB>
+__device__ __forceinline__ void mma_decoded(float (&acc)[4], const DecodedUnit<KB>& du, const uint8_t* xg,
+                                            bool xok) {
+  constexpr int NKB = kSpanK / KB;
+  constexpr int NMMA = KB / 16;
+  uint32_t xr[NKB][KB / 8];
+#pragma unroll
+  for (int j = 0; j < NKB; ++j) {
+#pragma unroll
+    for (int q = 0; q < KB / 32; ++q) {
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (xok) v = ld_x_v4(xg + j * (KB * 2) + 16 * q);
+      xr[j][4 * q + 0] = v.x; xr[j][4 * q + 1] = v.y; xr[j][4 * q + 2] = v.z; xr[j][4 * q + 3] = v.w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NKB; ++j) {
+    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int s = 0; s < NMMA; ++s) mma16816(d, du.a[j][s], xr[j][2 * s], xr[j][2 * s + 1]);
+    acc[0] = fmaf(du.sk0[j], d[0], acc[0]);
+    acc[1] = fmaf(du.sk0[j], d[1], acc[1]);
+    acc[2] = fmaf(du.sk1[j], d[2], acc[2]);
+    acc[3] = fmaf(du.sk1[j], d[3], acc[3]);
+  }
+}
+
+}  // namespace w4

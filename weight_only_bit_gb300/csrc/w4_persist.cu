@@ -1,40 +1,51 @@
-// w4_persist.cu -- fused 4-bit dequant-GEMV on CUDA cores (batches 1 ... 31), one persistent,
-// warp-specialised kernel for a single GEMV or for every GEMV of a decode step (sm_103a).
+// w4_persist.cu -- fused 4-bit dequant-GEMV for batches 1 ... 8 (sm_103a): one persistent,
+// warp-specialised kernel for a single GEMV or for every GEMV of a decode step.
 //
 // Computes y[m][n] = sum_k w_hat[n][k] * x[m][k] with w_hat decoded on chip, FP32 accumulation and
 // an FP16 result; no dequantised matrix ever reaches DRAM ("LLM Quantization on RTX 4060: Where
 // 4-bit Decode Falls Behind FP16", sections "Fused Kernel: Moving Dequantization On-Chip" and
 // "Kernel Implementation").
 //
-// Work: each GEMV is cut into tiles of whole rows (rows are contiguous in memory, so a tile is one
-// span).  GEMVs are grouped into levels; a level's GEMVs are independent of each other (the
-// projections of one decode layer that read the same activation: q, k, v / o / gate, up / down).
-// A level's x is read only after every tile of the previous level is complete, which models the
-// decode step's data dependencies ("Do Quantization and Sparsity make LLM Inference Faster ?",
-// section "What we did": the 197 GEMVs of one step).  Level 0 waits for the previous kernel in the
-// stream (programmatic dependent launch); later levels wait on tile counters in global memory.
-// Tile t of a level goes to CTA t mod gridDim.x; the grid is one CTA per SM, all co-resident.
+// Work: each GEMV is cut into tiles of whole rows.  GEMVs are grouped into levels; a level's GEMVs
+// are independent of each other (the projections of one decode layer that read the same
+// activation: q, k, v / o / gate, up / down).  A level's x is read only after every tile of the
+// previous level is complete, which models the decode step's data dependencies ("Do Quantization
+// and Sparsity make LLM Inference Faster ?", section "What we did": the 197 GEMVs of one step).
+// Level 0 waits for the previous kernel in the stream (programmatic dependent launch); later levels
+// wait on counters in global memory.  Tile t of a level goes to CTA t mod gridDim.x; the grid is
+// one CTA per SM, all co-resident.
 //
+// The arithmetic runs on the tensor cores through warp-level mma.sync.m16n8k16 (FP16 x FP16 ->
+// FP32), with the weights as the A operand and x (batch rows 0 ... 7, zero above the batch) as B:
+//   * a warp's unit of work is 16 rows x 256 k of one tile (a "span"): per 64-k block (32-k block
+//     when the scale block is 32) lane (g, t) = (lane / 4, lane % 4) reads the 8 (4) consecutive
+//     packed bytes 8t ... 8t + 7 of the rows its MMA rows g and g + 8 stand for (tile rows 2g and
+//     2g + 1 of the row group with 64-k blocks, g and g + 8 with 32-k blocks, the pairing that keeps
+//     the swizzled loads conflict-free); each byte is one A-fragment register, two
+//     consecutive k of one row, decoded by one shared-memory lookup in a byte-pair table (NF4 code
+//     values, q - 8 for INT4, E2M1 values for FP4, all exact in FP16 except the NF4 code values,
+//     which are rounded to FP16).  K is permuted identically in A and B, so the B fragment is the
+//     lane's own x elements, loaded in natural order;
+//   * the MMAs of one scale block start from zero, and the block's scale (FP32 absmax for NF4,
+//     FP16 scale for INT4 and FP4) multiplies the result into the unit's FP32 accumulators;
+//   * each unit leaves one FP32 partial per (batch row, weight row, span) in shared memory, and the
+//     reducer warp sums a row's spans in a fixed order (span 0, 1, 2, ...).  The split of K into
+//     spans depends only on K, so a row gets the same bits whatever the tiling.
 // Roles in a CTA:
-//   * producer warp: streams each tile's packed bytes and scales into a shared-memory ring of up to
-//     eight stages with 1-D bulk async copies (TMA unit), mbarrier completion and an L2 evict-first
-//     hint.  Weights never depend on other GEMVs, so it runs ahead across level boundaries and
-//     prefetches later levels.  It issues copies only while its consumers compute (a stream gate
-//     opened once a level's x is loaded and closed when the CTA's last tile of the level is
-//     reduced): DRAM traffic during the grid-wide wait between levels multiplies that wait.  At
-//     most three copies are in flight, which already saturates DRAM;
-//   * consumer warps: thread (rho, chunk) owns one 32-weight column chunk, loads that slice of x
-//     (through L1, which merges the requests of the threads sharing it) into registers for the
-//     whole level, and produces one partial sum per (row, chunk), two rows at a time, into one of
-//     two partial-sum buffers;
-//   * reducer warp: sums each row's partials in a fixed order (eight interleaved sequences, then a
-//     fixed tree, over 1, 2, 4 or 8 lanes per row with warp shuffles: the reduction idiom of "Do
-//     Quantization and Sparsity make LLM Inference Faster ?", "Optional: what does the custom
-//     kernel actually do?"), writes y, and after the CTA's last tile of a level publishes
-//     completion with one release.  The order depends only on K, so a row gets the same bits
-//     whatever the tiling.  Each lane issues a whole batch of loads before its first add: the
-//     shared-memory queue is long while consumers decode, so one round trip per tile, not one per
-//     partial, keeps the reducer ahead of the consumers.
+//   * producer warp: copies each tile into a shared-memory ring with one 2-D TMA tensor copy per span
+//     (a box of 128 bytes x the tile's rows, 128-byte swizzled: the 16-byte chunk c of tile row r
+//     lands at chunk c ^ (r & 7), so the fragment loads of a warp hit distinct banks) and its scales
+//     with one 1-D bulk copy, completion on the stage's mbarrier.  Weights never depend on other
+//     GEMVs, so it runs ahead across level boundaries.  Copies other than a level's first tile are
+//     issued only while the CTA's consumers compute (a stream gate opened once a level starts and
+//     closed before the stage of the CTA's last tile of the level is released), because data
+//     arriving at the SM while a level's completion is published and the next level waits slows
+//     that release and its polls; the first tile of a level is never held back, since the
+//     consumers wait for it before they wait for the previous level;
+//   * 14 consumer warps (16 warps in all, so each thread may hold 128 registers): the units of each tile, round-robin over the warps (continuing across
+//     tiles, so an uneven tile does not always load the same warps);
+//   * reducer warp: sums each row's partials, writes y, and after the CTA's last tile of a level
+//     publishes completion with one release.
 // Every wait is bounded in wall-clock time; a lost wait is recorded in the device error word and
 // the kernel runs to its end without further waiting.
 #include <cstdint>
@@ -43,44 +54,48 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "w4.h"
 #include "w4_common.cuh"
 #include "w4_decode.cuh"
 #include "w4_internal.h"
+#include "w4_mma_unit.cuh"
 
 namespace w4 {
 
 constexpr int kMaxStages = 8;
-constexpr int kMaxInFlight = 3;         // copies outstanding per CTA: enough for full DRAM bandwidth
-constexpr int kMaxConsumers = 320;      // longest row served: 320 chunks (K = 10240)
-constexpr int kStageTarget = 65536;     // packed bytes per stage (about): large tiles amortise each
-                                        // tile's barrier round trips; smaller when the ring won't fit
-constexpr int kRedBufs = 2;             // partial-sum buffers: the reducer may lag one tile
-constexpr int kRedCapFloats = 8192;     // largest partial-sum buffer (floats)
-constexpr int kXDigitCap = 40960;       // largest INT4 x digit table shared in shared memory (bytes)
+constexpr int kMaxInFlight = 3;        // tile copies outstanding per CTA
+constexpr int kConsumerWarps = 14;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;   // consumers, producer, reducer
+constexpr int kStageTarget = 65536;    // packed bytes per stage (about); smaller when the ring won't fit
+constexpr int kRedBufs = 2;            // partial-sum buffers: the reducer may lag one tile
+constexpr int kRedCapFloats = 12288;   // largest partial-sum buffer (floats)
 constexpr int kSmemCap = 227 * 1024;
+constexpr int kMaxRowsPerTile = 256;  // TMA box rows
+constexpr int kPrefetchTiles = 2;      // L2 prefetch distance, in the CTA's tiles
+constexpr bool kDecodeAhead = false;   // decode a warp's first unit of a level before that level's wait
 
-// Consumer warps per CTA by batch block: as many as the registers of one SM allow.
-__host__ __device__ constexpr int cons_warps(int MB) { return MB <= 1 ? 18 : MB == 2 ? 16 : 10; }
-
-// Lanes of the reducer warp per output row: all of a tile's outputs in one pass when possible.
-__host__ __device__ inline int red_lanes(int outs) {
-  int q = 8;
-  while (q > 1 && outs * q > 32) q >>= 1;
-  return q;
-}
-
-// Row stride (floats) of a partial-sum buffer: at least cpr and an odd multiple of Q, so the
-// (row, lane) reads of one reducer pass fall in 32 distinct banks.
-__host__ __device__ inline int red_stride(int cpr, int Q) { return cpr + ((Q - cpr) & (2 * Q - 1)); }
+__host__ __device__ constexpr int span_count(int K) { return (K + kSpanK - 1) / kSpanK; }
+__host__ __device__ constexpr int box_count(int K) { return (K + kBoxK - 1) / kBoxK; }
+// Shared-memory bytes of one TMA box of a tile of `rows` rows: whole 1 KB swizzle atoms (8 rows of
+// 128 bytes; the 128-byte swizzle wants 1 KB aligned boxes).
+__host__ __device__ constexpr int span_slot(int rows) { return ((rows + 7) / 8) * 1024; }
+// A stage: the boxes of a tile, then 1 KB that the last row group may read past the last box (its
+// rows beyond the tile are never used).
+__host__ __device__ constexpr int stage_bytes(int nbox, int rows) { return nbox * span_slot(rows) + 1024; }
+// Floats per (batch row, weight row) in a partial-sum buffer: at least the span count and 4 more
+// than a multiple of 8, so that the reducer's 16-byte loads of eight rows hit distinct banks.
+__host__ __device__ constexpr int part_stride(int C) { return C + ((4 - C) & 7); }
 
 struct PGemv {
   const uint8_t* packed;
   const void* scales;
   const __half* x;
   __half* y;
+  const CUtensorMap* tmap; // packed [N][K/2], box 128 bytes x rpt rows (device memory; null: map1)
   int N, K, bs, rpt;       // rpt: rows per tile
   int tile0, ntiles, srb;  // global tile range; scale bytes per row
-  int cpr;                 // chunks per row (K / 32)
+  int nspan, nbox, slot, cp;  // spans (128 k) and TMA boxes (256 k) per row; shared bytes per box;
+                              // partial stride (floats)
 };
 
 struct PLevel {
@@ -89,31 +104,30 @@ struct PLevel {
 
 template <int MAXL, int MAXG>
 struct PParams {
-  const float* codebook;
+  CUtensorMap map1;        // the tensor map of a single-GEMV launch
+  const float* codebook;   // NF4 code book (format 0)
   unsigned int* counters;  // [nlevels + 1] when nlevels > 1, else null
+  int fmt;                 // 0 NF4 (FP32 absmax), 1 INT4 (FP16 scale), 2 FP4 E2M1 (FP16 scale)
   int nlevels, ngemvs, M, inject_timeout;
-  int stages, stage_w, stage_s, red_floats, n_consumer_warps;
-  int xd_bytes;            // INT4: shared x digit table (0: every thread converts its slice)
+  int stages, stage_w, stage_s, red_floats;
   PLevel lv[MAXL];
   PGemv gm[MAXG];
 };
 
 struct PLayout {
-  int lut, xd, w, s, red, bar, total;
+  int lut, w, s, red, bar, total;
 };
 
-__host__ __device__ inline PLayout playout(int fmt, int stages, int stage_w, int stage_s, int red_floats,
-                                           int xd_bytes) {
+__host__ __device__ inline PLayout playout(int stages, int stage_w, int stage_s, int red_floats) {
   PLayout L;
   int off = 0;
-  L.lut = 0;
-  if (fmt == 0) off += kLutBytes;
-  L.xd = off;
-  off += (xd_bytes + 15) & ~15;   // bulk copies into the ring need 16-byte alignment
+  L.lut = off;
+  off += kLutBytes;           // 32 KB: the ring starts 1 KB aligned
   L.w = off;
   off += stages * stage_w;
   L.s = off;
   off += stages * stage_s;
+  off = (off + 15) & ~15;
   L.red = off;
   off += kRedBufs * red_floats * 4;
   off = (off + 15) & ~15;
@@ -129,16 +143,16 @@ __device__ __forceinline__ int first_owned(int tile0) {
   return tile0 + (((b - tile0) % G) + G) % G;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Adds v with release semantics at GPU scope: every write ordered before it (this thread's, and
 // its warp's through a preceding __syncwarp) is visible to a thread that acquires the new value.
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Bounded wait until *p >= target (other CTAs' releases).  Polls back to back for the first
@@ -169,71 +183,66 @@ __device__ __forceinline__ bool wait_gate(volatile int* gate, uint32_t site) {
   return false;
 }
 
-// Sum of one row's cpr partials rr[0 .. cpr) in the fixed order: sequence i (i < 8) adds
-// rr[i], rr[i + 8], rr[i + 16], ... from zero; the eight sums combine as
-// ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)).  Q lanes share the row (lane q holds the
-// sequences q, q + Q, ...); every lane of the group returns the same value, bit for bit, for any Q.
-// Loads go out in batches of 48 per lane before the adds that consume them.
-template <int Q>
-__device__ __forceinline__ float reduce_row(const float* rr, int cpr, int q) {
-  constexpr int U = 8 / Q;
-  constexpr int R = 48 / U;    // rounds of eight partials per batch
-  float a[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) a[u] = 0.0f;
-  int c0 = 0;
-  for (; c0 + 8 * R <= cpr; c0 += 8 * R) {   // full batches
-    float v[R][U];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int u = 0; u < U; ++u) v[r][u] = rr[c0 + 8 * r + q + Q * u];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int u = 0; u < U; ++u) a[u] += v[r][u];
-  }
-  if (c0 < cpr) {                             // the ragged last batch
-    float v[R][U];
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = c0 + 8 * r + q + Q * u;
-        v[r][u] = i < cpr ? rr[i] : 0.0f;
-      }
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (c0 + 8 * r + q + Q * u < cpr) a[u] += v[r][u];
-      }
-  }
-  if constexpr (Q == 1) {
-    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-  } else {
-    // pairs (s0 + s1), (s2 + s3), ...: the partner sequence is one lane away
-#pragma unroll
-    for (int u = 0; u < U; ++u) a[u] += __shfl_xor_sync(0xffffffffu, a[u], 1);
-    if constexpr (Q == 2) {
-      return (a[0] + a[1]) + (a[2] + a[3]);
-    } else {
-#pragma unroll
-      for (int u = 0; u < U; ++u) a[u] += __shfl_xor_sync(0xffffffffu, a[u], 2);
-      if constexpr (Q == 4) {
-        return a[0] + a[1];
-      } else {
-        return a[0] + __shfl_xor_sync(0xffffffffu, a[0], 4);
-      }
-    }
-  }
+// Asks L2 to fetch [p, p + bytes) from DRAM (no data to the SM).  The range is trimmed inwards to
+// 16-byte boundaries, so nothing outside it is touched.
+__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uintptr_t lo = (a + 15) & ~(uintptr_t)15, hi = (a + bytes) & ~(uintptr_t)15;
+  if (hi > lo)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
 }
 
-template <int FMT, int MB, int MAXL, int MAXG>
-__global__ void __launch_bounds__((cons_warps(MB) + 2) * 32, 1)
-    w4_persistent_kernel(const __grid_constant__ PParams<MAXL, MAXG> p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const PLayout Lo = playout(FMT, p.stages, p.stage_w, p.stage_s, p.red_floats, p.xd_bytes);
+// 2-D TMA tensor copy global -> shared (box at coordinates c0 = byte column, c1 = row); completion
+// adds the box's bytes to `bar`.  dst: 1 KB aligned shared address.
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                       uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+
+// The tiles of one CTA, in order across levels: level, GEMV and global tile index.
+template <int MAXL, int MAXG>
+struct TileCursor {
+  int L, g, t;
+  __device__ __forceinline__ void start(const PParams<MAXL, MAXG>& p) {
+    L = 0;
+    g = 0;
+    t = 0;
+    seek(p);
+  }
+  // from level L on: this CTA's first tile of the first level that has one
+  __device__ __forceinline__ void seek(const PParams<MAXL, MAXG>& p) {
+    while (L < p.nlevels) {
+      t = first_owned(p.lv[L].tile0);
+      if (t < p.lv[L].tile0 + p.lv[L].ntiles) break;
+      ++L;
+    }
+    if (L < p.nlevels) {
+      g = p.lv[L].gemv0;
+      while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
+    }
+  }
+  __device__ __forceinline__ bool valid(const PParams<MAXL, MAXG>& p) const { return L < p.nlevels; }
+  __device__ __forceinline__ void next(const PParams<MAXL, MAXG>& p) {
+    t += (int)gridDim.x;
+    if (t >= p.lv[L].tile0 + p.lv[L].ntiles) {
+      ++L;
+      seek(p);
+      return;
+    }
+    while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
+  }
+};
+
+template <int KB, bool SC32, int MAXL, int MAXG>
+__global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid_constant__ PParams<MAXL, MAXG> p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const PLayout Lo = playout(p.stages, p.stage_w, p.stage_s, p.red_floats);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lo.bar);
   uint64_t* empty = full + kMaxStages;
   uint64_t* rfull = empty + kMaxStages;
@@ -242,18 +251,17 @@ __global__ void __launch_bounds__((cons_warps(MB) + 2) * 32, 1)
   volatile int* gate = reinterpret_cast<volatile int*>(rfree + kRedBufs);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ncw = p.n_consumer_warps;
-  const int n_cons = ncw * 32;
+  const int n_cons = kConsumerWarps * 32;
   const int G = (int)gridDim.x;
   const int NS = p.stages;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], ncw);
+      mbar_init(&empty[i], kConsumerWarps);
     }
     for (int i = 0; i < kRedBufs; ++i) {
-      mbar_init(&rfull[i], ncw);
+      mbar_init(&rfull[i], kConsumerWarps);
       mbar_init(&rfree[i], 1);
     }
     *gate = 1;
@@ -262,49 +270,73 @@ __global__ void __launch_bounds__((cons_warps(MB) + 2) * 32, 1)
   __syncthreads();
   pdl_launch_dependents();
 
-  if (warp == ncw) {
+  if (warp == kConsumerWarps) {
     // ================================================================ producer warp
     if (p.inject_timeout) return;   // test hook: nothing issued, nothing in flight
     const uint64_t pol = policy_evict_first();
+    // L2 prefetch cursor, kPrefetchTiles ahead of the copies
+    TileCursor<MAXL, MAXG> pc;
+    pc.start(p);
+    auto prefetch_tile = [&](const TileCursor<MAXL, MAXG>& c) {
+      const PGemv& gm = p.gm[c.g];
+      const int r0 = (c.t - gm.tile0) * gm.rpt;
+      const int nrows = min(gm.rpt, gm.N - r0);
+      prefetch_l2(gm.packed + (size_t)r0 * (gm.K / 2), (size_t)nrows * (gm.K / 2));
+      prefetch_l2(reinterpret_cast<const uint8_t*>(gm.scales) + (size_t)r0 * gm.srb, (size_t)nrows * gm.srb);
+    };
+    if (lane == 0) {
+      for (int i = 0; i < kPrefetchTiles && pc.valid(p); ++i, pc.next(p)) prefetch_tile(pc);
+    }
+    TileCursor<MAXL, MAXG> cur;
+    cur.start(p);
     int j = 0;
+    int prev_level = -1;
     bool ok = true;
-    for (int L = 0; L < p.nlevels; ++L) {
-      const PLevel lv = p.lv[L];
-      int g = lv.gemv0;
-      for (int t = first_owned(lv.tile0); t < lv.tile0 + lv.ntiles; t += G, ++j) {
-        while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
-        const PGemv gm = p.gm[g];
-        const int st = j % NS;
-        const int round = j / NS;
-        // Prefetch of the first NS tiles may overlap the previous kernel in the stream; the
-        // bounded waits start only once that kernel is complete.
-        if (round == 1 && st == 0) pdl_wait();
-        if (lane == 0 && round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1, 0x201);
-        if (lane == 0 && ok) ok = wait_gate(gate, 0x20a);
-        if (lane == 0 && NS > kMaxInFlight && j >= kMaxInFlight && ok) {
-          const int jd = j - kMaxInFlight;
-          ok = mbar_wait(&full[jd % NS], (jd / NS) & 1, 0x209);
-        }
-        const int r0 = (t - gm.tile0) * gm.rpt;
-        const int nrows = min(gm.rpt, gm.N - r0);
-        const uint32_t wbytes = (uint32_t)nrows * (uint32_t)(gm.K / 2);
-        const uint32_t sbytes = (uint32_t)nrows * (uint32_t)gm.srb;
-        const uint32_t sbulk = sbytes & ~15u;
-        uint8_t* dst_w = smem + Lo.w + st * p.stage_w;
-        uint8_t* dst_s = smem + Lo.s + st * p.stage_s;
-        const uint8_t* src_s = reinterpret_cast<const uint8_t*>(gm.scales) + (size_t)r0 * gm.srb;
-        if (lane == 0) {
-          if (ok) {
-            for (uint32_t b = sbulk; b < sbytes; ++b) dst_s[b] = src_s[b];   // sub-16-byte tail
-            mbar_arrive_expect_tx(&full[st], wbytes + sbulk);
-            bulk_g2s(dst_w, gm.packed + (size_t)r0 * (gm.K / 2), wbytes, &full[st], pol);
-            if (sbulk) bulk_g2s(dst_s, src_s, sbulk, &full[st], pol);
-          } else {
-            mbar_arrive(&full[st]);
-          }
-        }
-        __syncwarp();
+    for (; cur.valid(p); cur.next(p), ++j) {
+      const PGemv& gm = p.gm[cur.g];
+      const int st = j % NS;
+      const int round = j / NS;
+      // Copies of the first NS tiles may overlap the previous kernel in the stream; the bounded
+      // waits start only once that kernel is complete.
+      if (round == 1 && st == 0) pdl_wait();
+      if (lane == 0 && round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1, 0x201);
+      // the gate holds back every tile but the first of a level: the consumers wait for that one
+      // before they wait for the previous level (and reopen the gate)
+      if (lane == 0 && ok && cur.L == prev_level) ok = wait_gate(gate, 0x20a);
+      prev_level = cur.L;
+      if (lane == 0 && NS > kMaxInFlight && j >= kMaxInFlight && ok) {
+        const int jd = j - kMaxInFlight;
+        ok = mbar_wait(&full[jd % NS], (jd / NS) & 1, 0x209);
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      const int r0 = (cur.t - gm.tile0) * gm.rpt;
+      const int nrows = min(gm.rpt, gm.N - r0);
+      const uint32_t sbytes = (uint32_t)nrows * (uint32_t)gm.srb;
+      const uint32_t sbulk = sbytes & ~15u;
+      const uint32_t dst_w = smem_u32(smem + Lo.w + st * p.stage_w);
+      uint8_t* dst_s = smem + Lo.s + st * p.stage_s;
+      const uint8_t* src_s = reinterpret_cast<const uint8_t*>(gm.scales) + (size_t)r0 * gm.srb;
+      const CUtensorMap* tm = gm.tmap ? gm.tmap : &p.map1;
+      if (lane == 0) {
+        if (ok) {
+          for (uint32_t b = sbulk; b < sbytes; ++b) dst_s[b] = src_s[b];   // sub-16-byte tail
+          // every box carries rpt rows (zeros past the matrix)
+          mbar_arrive_expect_tx(&full[st], (uint32_t)gm.nbox * (uint32_t)gm.rpt * 128u + sbulk);
+          if (pc.valid(p)) {
+            prefetch_tile(pc);
+            pc.next(p);
+          }
+        } else {
+          mbar_arrive(&full[st]);
+        }
+      }
+      __syncwarp();
+      if (ok) {
+        for (int c = lane; c < gm.nbox; c += 32)
+          tma_2d(dst_w + (uint32_t)(c * gm.slot), tm, c * (kBoxK / 2), r0, &full[st], pol);
+        if (lane == 31 && sbulk) bulk_g2s(dst_s, src_s, sbulk, &full[st], pol);
+      }
+      __syncwarp();
     }
     // never leave while bulk copies into this CTA's shared memory may be in flight
     if (lane == 0) {
@@ -315,51 +347,35 @@ __global__ void __launch_bounds__((cons_warps(MB) + 2) * 32, 1)
 
   float* red_base = reinterpret_cast<float*>(smem + Lo.red);
 
-  if (warp == ncw + 1) {
+  if (warp == kConsumerWarps + 1) {
     // ================================================================ reducer warp
     pdl_wait();   // counters are touched only after the previous kernel in the stream completed
+    TileCursor<MAXL, MAXG> cur;
+    cur.start(p);
     int j = 0;
     bool ok = true;
-    for (int L = 0; L < p.nlevels; ++L) {
-      const PLevel lv = p.lv[L];
-      int g = lv.gemv0;
-      const int t_end = lv.tile0 + lv.ntiles;
-      for (int t = first_owned(lv.tile0); t < t_end; t += G, ++j) {
-        while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
-        const PGemv gm = p.gm[g];
-        const int b = j % kRedBufs;
-        if (ok) ok = mbar_wait(&rfull[b], (j / kRedBufs) & 1, 0x203);
-        const int r0 = (t - gm.tile0) * gm.rpt;
-        const int nrows = min(gm.rpt, gm.N - r0);
-        const float* red = red_base + b * p.red_floats;
-        // output o = m * nrows + lr is buffer row o; Q lanes per output
-        const int outs = nrows * MB;
-        const int Q = red_lanes(outs);
-        const int stride = red_stride(gm.cpr, Q);
-        const int q = lane & (Q - 1);
-        for (int o0 = 0; o0 < outs; o0 += 32 / Q) {
-          const int o = o0 + lane / Q;
-          const int oc = o < outs ? o : outs - 1;
-          const float* rr = red + oc * stride;
-          float v;
-          switch (Q) {
-            case 8: v = reduce_row<8>(rr, gm.cpr, q); break;
-            case 4: v = reduce_row<4>(rr, gm.cpr, q); break;
-            case 2: v = reduce_row<2>(rr, gm.cpr, q); break;
-            default: v = reduce_row<1>(rr, gm.cpr, q); break;
-          }
-          const int m = oc / nrows;
-          if (o < outs && q == 0 && m < p.M) gm.y[(size_t)m * gm.N + r0 + (oc - m * nrows)] = __float2half_rn(v);
-        }
-        const bool publish = p.counters && t + G >= t_end;   // this CTA's last tile of level L
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&rfree[b]);
-          if (publish) {
-            if (L + 1 < p.nlevels) *gate = 0;   // before the release: the next level reopens it
-            red_release_add(&p.counters[L], 1u);
-          }
-        }
+    for (; cur.valid(p); ++j) {
+      const int L = cur.L;
+      const PGemv gm = p.gm[cur.g];
+      const int t = cur.t;
+      const int b = j % kRedBufs;
+      if (ok) ok = mbar_wait(&rfull[b], (j / kRedBufs) & 1, 0x203);
+      const int r0 = (t - gm.tile0) * gm.rpt;
+      const int nrows = min(gm.rpt, gm.N - r0);
+      const float* red = red_base + b * p.red_floats;
+      // output o = m * nrows + r: partials red[o * cp ... + nspan)
+      const int outs = nrows * p.M;
+      for (int o = lane; o < outs; o += 32) {
+        const float v = sum_spans(red + o * gm.cp, gm.nspan);
+        const int m = o / nrows;
+        gm.y[(size_t)m * gm.N + r0 + (o - m * nrows)] = __float2half_rn(v);
+      }
+      cur.next(p);
+      const bool publish = p.counters && cur.L != L;   // this CTA's last tile of level L
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&rfree[b]);
+        if (publish) red_release_add(&p.counters[L], 1u);
       }
     }
     // end of the launch: the last CTA to finish resets the counters for the next launch
@@ -376,127 +392,218 @@ __global__ void __launch_bounds__((cons_warps(MB) + 2) * 32, 1)
 
   // ================================================================== consumer warps
   const int tid = threadIdx.x;
+  build_lut(reinterpret_cast<uint32_t*>(smem + Lo.lut), p.fmt, p.codebook, tid, n_cons);
+  asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");   // the table is read before the first level
   const uint32_t lut_lane = smem_u32(smem + Lo.lut) + (uint32_t)lane * 4u;
-  if (FMT == 0) build_nf4_lut(reinterpret_cast<uint32_t*>(smem + Lo.lut), p.codebook, tid, n_cons);
-
-  constexpr int kTarget = cons_warps(MB) * 32;
-  XSlice<FMT, MB> xs;
-  const __half* x_loaded = nullptr;
-  int k_loaded = -1;
-  int rho = 0, chunk = 0, rps = 1;
-  bool active = false;
+  constexpr int RUN = KB / 8;
+  constexpr int NKB = kSpanK / KB;
+  const int g = lane >> 2, tq = lane & 3;
+  // this lane's byte offset of k block j of a span within a swizzled 128-byte box row: bytes
+  // 64 h + (KB/2) j + RUN t ... (h: which half of the box the span is) of tile row r sit in 16-byte
+  // chunk (64 h + (KB/2) j + RUN t) / 16 ^ (r & 7), i.e. the offset for h = 0 XOR (h << 6); the rows
+  // of MMA rows g and g + 8 have r & 7 = 2g & 7, 2g + 1 & 7 (64-k blocks) or g, g (32-k blocks)
+  uint32_t off0[NKB], off1[NKB];
+  {
+    const int x0 = KB == 64 ? (2 * g) & 7 : g, x1 = KB == 64 ? (2 * g + 1) & 7 : g;
+#pragma unroll
+    for (int jj = 0; jj < NKB; ++jj) {
+      const int byte = (KB / 2) * jj + RUN * tq;
+      off0[jj] = (uint32_t)((((byte >> 4) ^ x0) << 4) | (byte & 15));
+      off1[jj] = (uint32_t)((((byte >> 4) ^ x1) << 4) | (byte & 15));
+    }
+  }
   int j = 0;
+  int ubase = 0;            // units of this CTA's earlier tiles (round-robin continues across tiles)
   bool ok = true;
   bool pdl_done = false;
-  for (int L = 0; L < p.nlevels; ++L) {
-    const PLevel lv = p.lv[L];
-    const int t_first = first_owned(lv.tile0);
-    const int t_end = lv.tile0 + lv.ntiles;
-    if (t_first >= t_end) continue;           // no tile of this level here
-    // ---- wait until this level's inputs exist
-    if (!pdl_done) {
-      pdl_wait();
-      pdl_done = true;
+  TileCursor<MAXL, MAXG> cur;
+  cur.start(p);
+  int Lcur = -1;
+  for (; cur.valid(p); cur.next(p), ++j) {
+    const int L = cur.L;
+    const PGemv gm = p.gm[cur.g];
+    const int st = j % NS;
+    const int b = j % kRedBufs;
+    const int r0 = (cur.t - gm.tile0) * gm.rpt;
+    const int nrows = min(gm.rpt, gm.N - r0);
+    const int rgs = (nrows + 15) >> 4;
+    const int units = rgs * gm.nspan;
+    const bool full_last = (gm.K % kSpanK) == 0;   // every span full, scale runs aligned
+    const int lgbs = 31 - __clz(gm.bs);
+    const uint32_t tile_s = smem_u32(smem + Lo.w + st * p.stage_w);
+    const uint32_t stile_s = smem_u32(smem + Lo.s + st * p.stage_s);
+    float* red = red_base + b * p.red_floats;
+    // x of batch row g, in lanes whose batch row exists (the others' B columns are never stored)
+    const bool xok = g < p.M;
+    const uint8_t* xrow = reinterpret_cast<const uint8_t*>(gm.x + (size_t)min(g, p.M - 1) * gm.K) + (KB / 2) * tq;
+    // this warp's units u = u0, u0 + 14, ... of the tile as (row group rg, span c), stepped without
+    // divisions; MMA rows g and g + 8 stand for tile rows ra and rb of the row group
+    const int u0 = (warp - ubase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+    int rg = u0 / gm.nspan, c = u0 - rg * gm.nspan;
+    const int rsub_a = KB == 64 ? 2 * g : g, rsub_b = rsub_a + (KB == 64 ? 1 : 8);
+    bool first_done = false;
+    bool is_level_end;
+    {
+      TileCursor<MAXL, MAXG> nx = cur;
+      nx.next(p);
+      is_level_end = nx.L != L && nx.L < p.nlevels;
     }
-    if (L > 0 && p.counters) {
-      // every CTA that owns a tile of level L-1 adds one when it has finished them all
-      const unsigned owners = (unsigned)min(G, p.lv[L - 1].ntiles);
-      if (tid == 0 && ok) ok = wait_counter(&p.counters[L - 1], owners, 0x204);
-    }
-    // the level's start for all consumers (and the LUT complete at the first level): thread 0's
-    // acquire orders every consumer's reads of x after the previous level's writes
-    asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
-    int g = lv.gemv0;
-    PGemv gm = p.gm[g];
-    for (int t = t_first; t < t_end; t += G, ++j) {
-      if (t >= gm.tile0 + gm.ntiles) {
-        do { ++g; } while (t >= p.gm[g].tile0 + p.gm[g].ntiles);
-        gm = p.gm[g];
-      }
-      if (gm.x != x_loaded || gm.K != k_loaded) {
-        const int cpr = gm.cpr;
-        rps = cpr >= kTarget ? 1 : kTarget / cpr;
-        rho = tid / cpr;
-        chunk = tid - rho * cpr;
-        active = rho < rps;
-        bool shared_digits = false;
-        if constexpr (FMT == 1) {
-          if (t == t_first && p.M * cpr * 4 * kXDigitWords <= p.xd_bytes) {
-            // INT4: the threads of one row sweep (rho == 0) convert each chunk of x once and share
-            // the digits; the level-start barrier above ordered every read of the previous table
-            shared_digits = true;
-            uint32_t* xd = reinterpret_cast<uint32_t*>(smem + Lo.xd);
-            if (rho == 0 && active) {
-              load_x_slice<FMT, MB>(xs, gm.x, p.M, gm.K, chunk);
-              put_x_digits<MB>(xd, xs, p.M, cpr, chunk);
-            }
-            asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
-            if (rho > 0 && active) get_x_digits<MB>(xs, xd, p.M, cpr, chunk);
-          }
-        }
-        if (!shared_digits && active) load_x_slice<FMT, MB>(xs, gm.x, p.M, gm.K, chunk);
-        x_loaded = gm.x;
-        k_loaded = gm.K;
-      }
-      if (t == t_first && tid == 0) *gate = 1;
-      const int st = j % NS;
-      const int b = j % kRedBufs;
-      // every lane waits for itself: one instruction per warp, no broadcast round trip
+    if (L != Lcur) {
+      // ---- this CTA's first tile of the level: decode this warp's first unit of it before the
+      // wait for the previous level (weights never depend on it), wait, then multiply it by x
+      DecodedUnit<KB> du;
+      bool pre = false;
       if (ok) ok = mbar_wait(&full[st], (j / NS) & 1, 0x205);
-      if (j >= kRedBufs && ok) ok = mbar_wait(&rfree[b], ((j / kRedBufs) - 1) & 1, 0x206);
-      const int r0 = (t - gm.tile0) * gm.rpt;
-      const int nrows = min(gm.rpt, gm.N - r0);
-      const uint32_t sw = smem_u32(smem + Lo.w + st * p.stage_w);
-      const uint32_t ss = smem_u32(smem + Lo.s + st * p.stage_s);
-      float* red = red_base + b * p.red_floats;
-      const int stride = red_stride(gm.cpr, red_lanes(nrows * MB));
-      if (active && ok) {
-        const int es = FMT == 0 ? 4 : 2;
-        const uint32_t soff = (uint32_t)(((chunk * 32) / gm.bs) * es);
-        const uint32_t wrow = (uint32_t)(gm.K / 2);
-        int lr = rho;
-        for (; lr + rps < nrows; lr += 2 * rps) {   // two rows at once
-          const uint4 wv[2] = {lds128(sw + (uint32_t)lr * wrow + chunk * 16),
-                               lds128(sw + (uint32_t)(lr + rps) * wrow + chunk * 16)};
-          const uint32_t sa[2] = {ss + (uint32_t)(lr * gm.srb) + soff, ss + (uint32_t)((lr + rps) * gm.srb) + soff};
-          float part[2][MB];
-          chunk_dot<FMT, MB, 2>(part, wv, sa, lut_lane, xs);
+      if (kDecodeAhead && ok && full_last && u0 < units) {
+        const int ra = rg * 16 + rsub_a, rb = rg * 16 + rsub_b;
+        const uint32_t so = (uint32_t)(((c * kSpanK) >> lgbs) * (SC32 ? 4 : 2));
+        const uint32_t hm = (uint32_t)(c & 1) << 6;
+        uint32_t o0[NKB], o1[NKB];
 #pragma unroll
-          for (int m = 0; m < MB; ++m) {
-            red[(m * nrows + lr) * stride + chunk] = part[0][m];
-            red[(m * nrows + lr + rps) * stride + chunk] = part[1][m];
+        for (int jj = 0; jj < NKB; ++jj) { o0[jj] = off0[jj] ^ hm; o1[jj] = off1[jj] ^ hm; }
+        const uint32_t a0 = tile_s + (uint32_t)((c >> 1) * gm.slot + ra * 128), a1 = tile_s + (uint32_t)((c >> 1) * gm.slot + rb * 128);
+        const uint32_t s0a = stile_s + (uint32_t)(min(ra, nrows - 1) * gm.srb) + so;
+        const uint32_t s1a = stile_s + (uint32_t)(min(rb, nrows - 1) * gm.srb) + so;
+        const bool v0 = ra < nrows, v1 = rb < nrows;
+        pre = true;
+        if (KB == 32) {
+          if (lgbs == 5) decode_unit<KB, SC32, 4>(du, a0, a1, o0, o1, s0a, s1a, v0, v1, lut_lane);
+          else pre = false;
+        } else if (lgbs == 6) {
+          decode_unit<KB, SC32, 2>(du, a0, a1, o0, o1, s0a, s1a, v0, v1, lut_lane);
+        } else {
+          decode_unit<KB, SC32, 1>(du, a0, a1, o0, o1, s0a, s1a, v0, v1, lut_lane);
+        }
+      }
+      // ---- wait until this level's inputs exist
+      if (!pdl_done) {
+        pdl_wait();
+        pdl_done = true;
+      }
+      if (L > 0 && p.counters) {
+        // every CTA that owns a tile of level L-1 adds one when it has finished them all
+        const unsigned owners = (unsigned)min(G, p.lv[L - 1].ntiles);
+        if (tid == 0 && ok) ok = wait_counter(&p.counters[L - 1], owners, 0x204);
+      }
+      // the level's start for all consumers: thread 0's acquire orders every consumer's reads of
+      // x after the previous level's writes
+      asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
+      if (tid == 0) *gate = 1;
+      Lcur = L;
+      if (pre) {
+        if (j >= kRedBufs && ok) ok = mbar_wait(&rfree[b], ((j / kRedBufs) - 1) & 1, 0x206);
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_decoded<KB>(acc, du, xrow + c * (kSpanK * 2), xok);
+        if (ok) {
+          const int ra = rg * 16 + rsub_a, rb = rg * 16 + rsub_b;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int m = 2 * tq + q;
+            if (m < p.M) {
+              if (ra < nrows) red[(m * nrows + ra) * gm.cp + c] = acc[q];
+              if (rb < nrows) red[(m * nrows + rb) * gm.cp + c] = acc[2 + q];
+            }
           }
         }
-        if (lr < nrows) {
-          const uint4 wv[1] = {lds128(sw + (uint32_t)lr * wrow + chunk * 16)};
-          const uint32_t sa[1] = {ss + (uint32_t)(lr * gm.srb) + soff};
-          float part[1][MB];
-          chunk_dot<FMT, MB, 1>(part, wv, sa, lut_lane, xs);
-#pragma unroll
-          for (int m = 0; m < MB; ++m) red[(m * nrows + lr) * stride + chunk] = part[0][m];
+        first_done = true;
+      }
+    }
+    // every lane waits for itself: one instruction per warp, no broadcast round trip
+    if (ok) ok = mbar_wait(&full[st], (j / NS) & 1, 0x205);
+    if (j >= kRedBufs && ok) ok = mbar_wait(&rfree[b], ((j / kRedBufs) - 1) & 1, 0x206);
+    if (ok) {
+      const int sshift = 31 - __clz(gm.bs / KB);
+      int u = u0;
+      if (first_done) {
+        u += kConsumerWarps;
+        c += kConsumerWarps;
+        while (c >= gm.nspan) {
+          c -= gm.nspan;
+          ++rg;
         }
       }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&empty[st]);
-        mbar_arrive(&rfull[b]);
+      for (; u < units; u += kConsumerWarps) {
+        const int ra = rg * 16 + rsub_a, rb = rg * 16 + rsub_b;
+        const int rac = min(ra, nrows - 1), rbc = min(rb, nrows - 1);
+        const uint32_t a0 = tile_s + (uint32_t)((c >> 1) * gm.slot + ra * 128);
+        const uint32_t a1 = tile_s + (uint32_t)((c >> 1) * gm.slot + rb * 128);
+        const uint32_t hm = (uint32_t)(c & 1) << 6;
+        uint32_t o0[NKB], o1[NKB];
+#pragma unroll
+        for (int jj = 0; jj < NKB; ++jj) { o0[jj] = off0[jj] ^ hm; o1[jj] = off1[jj] ^ hm; }
+        const uint32_t s0a = stile_s + (uint32_t)(rac * gm.srb), s1a = stile_s + (uint32_t)(rbc * gm.srb);
+        const uint8_t* xg = xrow + c * (kSpanK * 2);
+        const int sidx0 = (c * kSpanK) >> lgbs;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const bool v0 = ra < nrows, v1 = rb < nrows;
+        if (full_last) {
+          // every span full, each row's span scales one aligned vector: max(1, 128 / bs) of them
+          const uint32_t so = (uint32_t)(sidx0 * (SC32 ? 4 : 2));
+          if (KB == 32) {
+            if (lgbs == 5) mma_unit<KB, SC32, 4>(acc, a0, a1, o0, o1, s0a + so, s1a + so, v0, v1, xg, xok, 0, 0, 0, lut_lane, lane);
+            else mma_unit<KB, SC32, 0>(acc, a0, a1, o0, o1, s0a, s1a, v0, v1, xg, xok, sidx0, sshift, kSpanK / KB, lut_lane, lane);
+          } else if (lgbs == 6) {
+            mma_unit<KB, SC32, 2>(acc, a0, a1, o0, o1, s0a + so, s1a + so, v0, v1, xg, xok, 0, 0, 0, lut_lane, lane);
+          } else {
+            mma_unit<KB, SC32, 1>(acc, a0, a1, o0, o1, s0a + so, s1a + so, v0, v1, xg, xok, 0, 0, 0, lut_lane, lane);
+          }
+        } else {
+          const int nkb = min(kSpanK, gm.K - c * kSpanK) / KB;
+          mma_unit<KB, SC32, 0>(acc, a0, a1, o0, o1, s0a, s1a, v0, v1, xg, xok, sidx0, sshift, nkb, lut_lane, lane);
+        }
+        // partials: batch rows 2t, 2t + 1 of weight rows ra and rb
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int m = 2 * tq + q;
+          if (m < p.M) {
+            if (ra < nrows) red[(m * nrows + ra) * gm.cp + c] = acc[q];
+            if (rb < nrows) red[(m * nrows + rb) * gm.cp + c] = acc[2 + q];
+          }
+        }
+        c += kConsumerWarps;
+        while (c >= gm.nspan) {
+          c -= gm.nspan;
+          ++rg;
+        }
       }
+    }
+    ubase += units;
+    __syncwarp();
+    if (lane == 0) {
+      // the CTA's last tile of a level: close the stream gate before this stage is released, so
+      // that no copy is issued (and in flight) while the level's completion is published and the
+      // next level waits; the next level's start reopens it
+      if (p.counters && is_level_end) *gate = 0;
+      mbar_arrive(&empty[st]);
+      mbar_arrive(&rfull[b]);
     }
   }
   asm volatile("bar.sync 2, %0;" ::"r"(n_cons + 32) : "memory");
 }
 
 // ====================================================================== host side
-static int g_sm_count = 0;
+// Per-device values the host side looks up once (SM counts; the kernels' attribute set-up and
+// occupancy): a fixed table indexed by device, guarded by one mutex.
+constexpr int kMaxDevices = 64;
+
+static int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
 
 int device_sm_count() {
-  if (g_sm_count == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sm_count <= 0) g_sm_count = 1;
+  static std::mutex mu;
+  static int sms[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (sms[dev] == 0) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 1;
   }
-  return g_sm_count;
+  return sms[dev];
 }
 
 static int gcd_int(int a, int b) {
@@ -504,42 +611,15 @@ static int gcd_int(int a, int b) {
   return a;
 }
 
-static int batch_block(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8; }
-
-// Partial-sum floats a tile of nr rows needs.
-static int red_floats_for(int MB, int cpr, int nr) {
-  const int outs = nr * MB;
-  return outs * red_stride(cpr, red_lanes(outs));
-}
-
-// Per-GEMV geometry that does not depend on the tiling.
+// Per-GEMV geometry: scale bytes per row, the row count that keeps every tile's scale span 16-byte
+// aligned, the largest tile, spans per row, partial stride and partial floats.
 struct GeomG {
-  int cpr, srb, align_rows, rpt_max, ncw, rps, red_need;
+  int srb, align_rows, rpt_max, nspan, nbox, cp, red_need;
 };
 
-static bool geom(int fmt, int MB, int K, int bs, int stage_target, GeomG& o) {
-  o.cpr = K / 32;
-  if (o.cpr < 1 || o.cpr > kMaxConsumers) return false;
-  const int target = cons_warps(MB) * 32;
-  const int rps = o.cpr >= target ? 1 : target / o.cpr;
-  o.ncw = (rps * o.cpr + 31) / 32;
-  o.srb = (K / bs) * (fmt == 0 ? 4 : 2);
-  o.align_rows = 16 / gcd_int(o.srb, 16);       // keeps every tile's scale span 16-byte aligned
-  o.rps = rps;
-  // about kStageTarget packed bytes, rounded to a whole number of consumer sweeps, within the
-  // partial-sum buffer's cap
-  const int r = stage_target / (K / 2);
-  int sweeps = (r + rps / 2) / rps;
-  if (sweeps < 1) sweeps = 1;
-  int rows = sweeps * rps;
-  while (rows > 1 && red_floats_for(MB, o.cpr, rows) > kRedCapFloats) rows = rows > rps ? rows - rps : rows - 1;
-  rows = (rows / o.align_rows) * o.align_rows;
-  if (rows < o.align_rows) rows = o.align_rows;
-  o.rpt_max = rows;
-  o.red_need = 1;
-  for (int nr = 1; nr <= rows; ++nr) o.red_need = max(o.red_need, red_floats_for(MB, o.cpr, nr));
-  return true;
-}
+static int kb_of(int bs) { return bs >= 64 ? 64 : 32; }
+
+static bool shape_ok(int K, int bs) { return K >= 32 && K % 32 == 0 && K <= W4_MAX_K && bs >= 32 && K % bs == 0; }
 
 struct Job {
   const uint8_t* packed;
@@ -549,30 +629,52 @@ struct Job {
   int N, K, bs, level;
 };
 
+// Rows per tile and its constraints for one GEMV at a stage budget (bytes of packed data).
+static void tile_rows(int fmt, int M, int K, int bs, int stage_target, GeomG& o) {
+  o.nspan = span_count(K);
+  o.nbox = box_count(K);
+  o.cp = part_stride(o.nspan);
+  o.srb = (K / bs) * (fmt == 0 ? 4 : 2);
+  o.align_rows = 16 / gcd_int(o.srb, 16);       // keeps every tile's scale span 16-byte aligned
+  int rows = stage_target / (o.nbox * 128);
+  if (rows > 16) rows &= ~15;                   // whole MMA row groups when the tile has several
+  rows = max(1, min(rows, kMaxRowsPerTile));
+  while (rows > 1 && rows * M * o.cp > kRedCapFloats) rows = rows > 16 ? rows - 16 : rows - 1;
+  rows = (rows / o.align_rows) * o.align_rows;
+  if (rows < o.align_rows) rows = o.align_rows;
+  o.rpt_max = rows;
+  o.red_need = rows * M * o.cp;
+}
+
 struct Plan {
-  int stage_target, stages, stage_w, stage_s, red_floats, ncw, xd_bytes;
+  int stage_target, stages, stage_w, stage_s, red_floats, kb;
   PLayout L;
 };
 
-// Layout of a set of GEMVs at batch block MB (independent of tiling, which never exceeds rpt_max):
+// Layout of a set of GEMVs at batch M (independent of the tiling, which never exceeds rpt_max):
 // the fixed parts, then as many ring stages (2 ... kMaxStages) as shared memory holds; the stage
-// size steps down from kStageTarget until two stages fit.
-static bool plan_layout(int fmt, int MB, int M, const Job* jobs, int n, Plan& P) {
+// size steps down from kStageTarget until two stages fit.  All GEMVs must share the k-block
+// width (scale blocks of 32, or of 64 and more).
+static bool plan_layout(int fmt, int M, const Job* jobs, int n, Plan& P) {
+  P.kb = kb_of(jobs[0].bs);
+  for (int i = 0; i < n; ++i)
+    if (kb_of(jobs[i].bs) != P.kb || !shape_ok(jobs[i].K, jobs[i].bs)) return false;
   for (P.stage_target = kStageTarget; P.stage_target >= 2048; P.stage_target = P.stage_target * 3 / 4) {
-    P.stage_w = 16; P.stage_s = 16; P.red_floats = 1; P.ncw = 1; P.xd_bytes = 0;
-    for (int i = 0; i < n; ++i) {
+    P.stage_w = 1024; P.stage_s = 16; P.red_floats = 4;
+    bool fits = true;
+    for (int i = 0; i < n && fits; ++i) {
       GeomG gg;
-      if (!geom(fmt, MB, jobs[i].K, jobs[i].bs, P.stage_target, gg)) return false;
-      P.stage_w = max(P.stage_w, gg.rpt_max * (jobs[i].K / 2));
+      tile_rows(fmt, M, jobs[i].K, jobs[i].bs, P.stage_target, gg);
+      if (gg.red_need > kRedCapFloats) fits = false;
+      P.stage_w = max(P.stage_w, stage_bytes(gg.nbox, gg.rpt_max));
       P.stage_s = max(P.stage_s, ((gg.rpt_max * gg.srb) + 15) & ~15);
       P.red_floats = max(P.red_floats, gg.red_need);
-      P.ncw = max(P.ncw, gg.ncw);
-      const int xd = M * gg.cpr * 4 * kXDigitWords;
-      if (fmt == 1 && xd <= kXDigitCap) P.xd_bytes = max(P.xd_bytes, xd);
     }
+    if (!fits) continue;
+    P.red_floats = (P.red_floats + 3) & ~3;
     for (P.stages = kMaxStages; P.stages >= 2; --P.stages) {
-      P.L = playout(fmt, P.stages, P.stage_w, P.stage_s, P.red_floats, P.xd_bytes);
-      if (P.L.total <= kSmemCap) return true;
+      P.L = playout(P.stages, P.stage_w, P.stage_s, P.red_floats);
+      if (P.L.total + 1024 <= kSmemCap) return true;   // + the 1 KB alignment slack
     }
   }
   return false;
@@ -582,7 +684,7 @@ int simt_max_batch(int format, int K, int bs) {
   Job jb{nullptr, nullptr, nullptr, nullptr, 1, K, bs, 0};
   for (int m : {8, 4, 2, 1}) {
     Plan P;
-    if (plan_layout(format, m, m, &jb, 1, P)) return m;
+    if (plan_layout(format, m, &jb, 1, P)) return m;
   }
   return 0;
 }
@@ -590,59 +692,46 @@ int simt_max_batch(int format, int K, int bs) {
 bool plan_simt(int format, int M, int K, int bs, SimtPlan* out) {
   const int mb = simt_max_batch(format, K, bs);
   if (mb < 1 || M < 1) return false;
-  // the widest launch: min(M, mb) rows on the batch block that covers them
+  // the widest launch: min(M, mb) batch rows
   const int mm = M < mb ? M : mb;
   Job jb{nullptr, nullptr, nullptr, nullptr, 1, K, bs, 0};
   Plan P;
-  if (!plan_layout(format, batch_block(mm), mm, &jb, 1, P)) return false;
+  if (!plan_layout(format, mm, &jb, 1, P)) return false;
   out->mb = mm;
   out->launches = (M + mb - 1) / mb;
-  out->threads = P.ncw * 32 + 64;
-  out->smem = P.L.total;
+  out->threads = kThreads;
+  out->smem = P.L.total + 1024;
   out->stages = P.stages;
   return true;
 }
 
-template <int FMT, int MB, int MAXL, int MAXG>
-static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float* codebook, unsigned* counters,
-                                     bool pdl, cudaStream_t stream) {
-  using P = PParams<MAXL, MAXG>;
-  auto kern = w4_persistent_kernel<FMT, MB, MAXL, MAXG>;
-  P* pp = new P();   // large parameter block: build on the heap
-  P& p = *pp;
+// Everything a launch needs, computed on the host: parameters (levels, GEMVs and their tiling), the
+// tensor map of each GEMV (box rows = its rows per tile), and the geometry.
+template <int MAXL, int MAXG>
+struct Prepared {
+  PParams<MAXL, MAXG> p;
+  CUtensorMap maps[MAXG];
+  Plan plan;
+  int grid;
+};
+
+template <int MAXL, int MAXG>
+static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* codebook, Prepared<MAXL, MAXG>& P) {
   int nlev = 0;
   for (int i = 0; i < n; ++i) nlev = max(nlev, jobs[i].level + 1);
-  if (n > MAXG || nlev > MAXL) { delete pp; return cudaErrorNotSupported; }
-  Plan plan;
-  if (!plan_layout(FMT, MB, M, jobs, n, plan)) {
-    delete pp;
-    return cudaErrorNotSupported;
-  }
-  static bool attr_done = false;   // one flag per instance
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
-    if (e != cudaSuccess) { delete pp; return e; }
-    attr_done = true;
-  }
-  const int threads = plan.ncw * 32 + 64;
-  static int occ_threads = -1, occ_smem = -1, occ_val = 1;
-  if (occ_threads != threads || occ_smem != plan.L.total) {
-    int v = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, (size_t)plan.L.total);
-    if (e != cudaSuccess) { delete pp; return e; }
-    occ_threads = threads; occ_smem = plan.L.total; occ_val = v < 1 ? 1 : (v > 2 ? 2 : v);
-  }
-  const int gmax = device_sm_count() * occ_val;
+  if (n < 1 || n > MAXG || nlev > MAXL) return cudaErrorNotSupported;
+  if (!plan_layout(fmt, M, jobs, n, P.plan)) return cudaErrorNotSupported;
+  const int gmax = device_sm_count();   // one CTA per SM: the ring is sized for the whole SM
+  PParams<MAXL, MAXG>& p = P.p;
   p.codebook = codebook;
-  p.counters = nlev > 1 ? counters : nullptr;
-  if (nlev > 1 && !counters) { delete pp; return cudaErrorInvalidValue; }
+  p.counters = nullptr;
+  p.fmt = fmt;
   p.nlevels = nlev;
   p.ngemvs = n;
   p.M = M;
-  p.inject_timeout = take_fault_injection();
-  p.stages = plan.stages; p.stage_w = plan.stage_w; p.stage_s = plan.stage_s; p.red_floats = plan.red_floats;
-  p.n_consumer_warps = plan.ncw;
-  p.xd_bytes = plan.xd_bytes;
+  p.inject_timeout = 0;
+  p.stages = P.plan.stages; p.stage_w = P.plan.stage_w; p.stage_s = P.plan.stage_s;
+  p.red_floats = P.plan.red_floats;
   // tiling, level by level: balanced tiles per CTA, rows per tile within each GEMV's stage budget
   int tile = 0, max_level_tiles = 0;
   for (int Lv = 0, i = 0; Lv < nlev; ++Lv) {
@@ -651,7 +740,7 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
     int rmin = 1 << 30;
     while (i < n && jobs[i].level == Lv) {
       GeomG gg;
-      geom(FMT, MB, jobs[i].K, jobs[i].bs, plan.stage_target, gg);
+      tile_rows(fmt, M, jobs[i].K, jobs[i].bs, P.plan.stage_target, gg);
       rows += jobs[i].N;
       rmin = min(rmin, gg.rpt_max);
       ++i;
@@ -662,25 +751,60 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
     const long long tpc = (rows + (long long)gmax * rmin - 1) / ((long long)gmax * rmin);
     for (int q = first; q < i; ++q) {
       GeomG gg;
-      geom(FMT, MB, jobs[q].K, jobs[q].bs, plan.stage_target, gg);
+      tile_rows(fmt, M, jobs[q].K, jobs[q].bs, P.plan.stage_target, gg);
       int rpt = (int)((rows + (long long)gmax * tpc - 1) / ((long long)gmax * tpc));
-      if (rpt > gg.rps) rpt = ((rpt + gg.rps - 1) / gg.rps) * gg.rps;   // whole sweeps when it can
+      if (rpt > 16) rpt = (rpt + 15) & ~15;                          // whole MMA row groups
       rpt = ((rpt + gg.align_rows - 1) / gg.align_rows) * gg.align_rows;
       rpt = min(rpt, gg.rpt_max);
       PGemv& g = p.gm[q];
       g.packed = jobs[q].packed; g.scales = jobs[q].scales; g.x = jobs[q].x; g.y = jobs[q].y;
+      g.tmap = nullptr;
       g.N = jobs[q].N; g.K = jobs[q].K; g.bs = jobs[q].bs; g.rpt = rpt;
-      g.tile0 = tile; g.ntiles = (g.N + rpt - 1) / rpt; g.srb = gg.srb; g.cpr = gg.cpr;
+      g.tile0 = tile; g.ntiles = (g.N + rpt - 1) / rpt; g.srb = gg.srb;
+      g.nspan = gg.nspan; g.nbox = gg.nbox; g.slot = span_slot(rpt); g.cp = gg.cp;
+      if (!encode_tmap_2d(&P.maps[q], 1, g.packed, g.K / 2, g.N, kBoxK / 2, rpt)) return cudaErrorNotSupported;
       tile += g.ntiles;
     }
     p.lv[Lv].ntiles = tile - p.lv[Lv].tile0;
     max_level_tiles = max(max_level_tiles, p.lv[Lv].ntiles);
   }
-  const int grid = nlev > 1 ? gmax : min(gmax, max_level_tiles);
+  P.grid = nlev > 1 ? gmax : min(gmax, max_level_tiles);
+  p.map1 = P.maps[0];
+  return cudaSuccess;
+}
+
+// Per-device, per-kernel-instance launch set-up (the shared-memory attribute), done once.
+struct KernelSetup {
+  std::mutex mu;
+  bool attr_done[kMaxDevices] = {};
+};
+
+// maps: device array of the n tensor maps (multi-GEMV launches) or null (single GEMV: map1).
+template <int KB, bool SC32, int MAXL, int MAXG>
+static cudaError_t launch_prepared(Prepared<MAXL, MAXG>& P, unsigned* counters, const CUtensorMap* maps, bool pdl,
+                                   cudaStream_t stream) {
+  auto kern = w4_persistent_kernel<KB, SC32, MAXL, MAXG>;
+  static KernelSetup setup;   // one per instance
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(setup.mu);
+    if (!setup.attr_done[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
+      if (e != cudaSuccess) return e;
+      setup.attr_done[dev] = true;
+    }
+  }
+  PParams<MAXL, MAXG>& p = P.p;
+  if (p.nlevels > 1 && !counters) return cudaErrorInvalidValue;
+  if (p.ngemvs > 1 && !maps) return cudaErrorInvalidValue;
+  p.counters = p.nlevels > 1 ? counters : nullptr;
+  for (int q = 0; q < p.ngemvs; ++q) p.gm[q].tmap = p.ngemvs > 1 ? maps + q : nullptr;
+  p.inject_timeout = take_fault_injection();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3((unsigned)threads);
-  cfg.dynamicSmemBytes = (size_t)plan.L.total;
+  cfg.gridDim = dim3((unsigned)P.grid);
+  cfg.blockDim = dim3((unsigned)kThreads);
+  cfg.dynamicSmemBytes = (size_t)P.plan.L.total + 1024;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -689,27 +813,19 @@ static cudaError_t launch_persistent(const Job* jobs, int n, int M, const float*
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   note_launch();
-  delete pp;
   return e;
 }
 
 template <int MAXL, int MAXG>
-static cudaError_t dispatch(int fmt, int MB, const Job* jobs, int n, int M, const float* codebook, unsigned* counters,
-                            bool pdl, cudaStream_t s) {
+static cudaError_t dispatch(int fmt, Prepared<MAXL, MAXG>& P, unsigned* counters, const CUtensorMap* maps, bool pdl,
+                            cudaStream_t s) {
+  const bool kb64 = P.plan.kb == 64;
   if (fmt == 0) {
-    switch (MB) {
-      case 1: return launch_persistent<0, 1, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
-      case 2: return launch_persistent<0, 2, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
-      case 4: return launch_persistent<0, 4, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
-      default: return launch_persistent<0, 8, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
-    }
+    if (kb64) return launch_prepared<64, true, MAXL, MAXG>(P, counters, maps, pdl, s);
+    return launch_prepared<32, true, MAXL, MAXG>(P, counters, maps, pdl, s);
   }
-  switch (MB) {
-    case 1: return launch_persistent<1, 1, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
-    case 2: return launch_persistent<1, 2, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
-    case 4: return launch_persistent<1, 4, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
-    default: return launch_persistent<1, 8, MAXL, MAXG>(jobs, n, M, codebook, counters, pdl, s);
-  }
+  if (kb64) return launch_prepared<64, false, MAXL, MAXG>(P, counters, maps, pdl, s);
+  return launch_prepared<32, false, MAXL, MAXG>(P, counters, maps, pdl, s);
 }
 
 cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scales, const float* codebook,
@@ -717,42 +833,68 @@ cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scal
                              cudaStream_t stream) {
   if (M < 1 || M > 8) return cudaErrorNotSupported;
   Job jb{packed, scales, x, y, N, K, bs, 0};
-  return dispatch<1, 1>(format, batch_block(M), &jb, 1, M, codebook, nullptr, pdl, stream);
+  Prepared<1, 1> P;
+  cudaError_t e = prepare<1, 1>(format, &jb, 1, M, codebook, P);
+  if (e != cudaSuccess) return e;
+  return dispatch<1, 1>(format, P, nullptr, nullptr, pdl, stream);
 }
 
-cudaError_t launch_step_simt(int format, const StepJob* jobs, int n, int M, const float* codebook, unsigned* counters,
-                             bool pdl, cudaStream_t stream) {
+using StepPrepared = Prepared<kStepMaxGemvs, kStepMaxGemvs>;
+
+static cudaError_t prepare_step(int format, const StepJob* jobs, int n, int M, const float* codebook, StepPrepared& P) {
   if (M < 1 || M > 8 || n < 1 || n > kStepMaxGemvs) return cudaErrorNotSupported;
   Job js[kStepMaxGemvs];
   for (int i = 0; i < n; ++i) {
     js[i] = Job{jobs[i].packed, jobs[i].scales, jobs[i].x, jobs[i].y, jobs[i].N, jobs[i].K, jobs[i].bs, jobs[i].level};
   }
-  return dispatch<kStepMaxGemvs, kStepMaxGemvs>(format, batch_block(M), js, n, M, codebook, counters, pdl, stream);
+  return prepare<kStepMaxGemvs, kStepMaxGemvs>(format, js, n, M, codebook, P);
+}
+
+cudaError_t step_simt_maps(int format, const StepJob* jobs, int n, int M, CUtensorMap* maps_out) {
+  StepPrepared* P = new StepPrepared();   // large: build on the heap
+  cudaError_t e = prepare_step(format, jobs, n, M, nullptr, *P);
+  if (e == cudaSuccess)
+    for (int i = 0; i < n; ++i) maps_out[i] = P->maps[i];
+  delete P;
+  return e;
+}
+
+cudaError_t launch_step_simt(int format, const StepJob* jobs, int n, int M, const float* codebook, unsigned* counters,
+                             const CUtensorMap* maps, bool pdl, cudaStream_t stream) {
+  StepPrepared* P = new StepPrepared();
+  cudaError_t e = prepare_step(format, jobs, n, M, codebook, *P);
+  if (e == cudaSuccess) e = dispatch<kStepMaxGemvs, kStepMaxGemvs>(format, *P, counters, maps, pdl, stream);
+  delete P;
+  return e;
 }
 
 // ---------------------------------------------------------------------------------------------
-// Counters for w4_gemv_levels_noalloc: a fixed array inside the library, for callers that cannot
-// allocate device memory.  In host code the name g_noalloc_counters is only a stand-in for the
-// device object; its device address is looked up once per device and cached.
+// Counters and tensor maps for w4_gemv_levels_noalloc: fixed arrays inside the library, for callers
+// that cannot allocate device memory.  In host code the names are only stand-ins for the device
+// objects; their device addresses are looked up once per device and cached.
 constexpr int kNoAllocMaxLevels = 256;
-constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned int g_noalloc_counters[kNoAllocMaxLevels + 1];
+static __device__ __align__(128) CUtensorMap g_noalloc_maps[kStepMaxGemvs];
 
-static cudaError_t noalloc_counters(unsigned** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+static cudaError_t noalloc_arrays(unsigned** counters, CUtensorMap** maps) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
   static std::mutex mu;
-  static unsigned* addr[kMaxDevices] = {};
+  static unsigned* caddr[kMaxDevices] = {};
+  static CUtensorMap* maddr[kMaxDevices] = {};
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_counters);   // with this device current
+  if (caddr[dev] == nullptr) {
+    void* pc = nullptr;
+    void* pm = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&pc, g_noalloc_counters);   // with this device current
     if (e != cudaSuccess) return e;
-    addr[dev] = static_cast<unsigned*>(p);
+    e = cudaGetSymbolAddress(&pm, g_noalloc_maps);
+    if (e != cudaSuccess) return e;
+    caddr[dev] = static_cast<unsigned*>(pc);
+    maddr[dev] = static_cast<CUtensorMap*>(pm);
   }
-  *out = addr[dev];
+  *counters = caddr[dev];
+  *maps = maddr[dev];
   return cudaSuccess;
 }
 
@@ -760,14 +902,20 @@ int noalloc_max_levels() { return kNoAllocMaxLevels; }
 
 cudaError_t launch_step_simt_noalloc(int format, const StepJob* jobs, int n, int M, const float* codebook,
                                      int nlevels, cudaStream_t stream) {
-  if (nlevels < 1 || nlevels > kNoAllocMaxLevels) return cudaErrorInvalidValue;
+  if (nlevels < 1 || nlevels > kNoAllocMaxLevels || n > kStepMaxGemvs) return cudaErrorInvalidValue;
   unsigned* counters = nullptr;
-  cudaError_t e = noalloc_counters(&counters);
+  CUtensorMap* maps = nullptr;
+  cudaError_t e = noalloc_arrays(&counters, &maps);
   if (e != cudaSuccess) return e;
-  // the array keeps the previous call's contents: start from zero
-  e = cudaMemsetAsync(counters, 0, sizeof(unsigned) * (size_t)(nlevels + 1), stream);
-  if (e != cudaSuccess) return e;
-  return launch_step_simt(format, jobs, n, M, codebook, counters, true, stream);
+  StepPrepared* P = new StepPrepared();
+  e = prepare_step(format, jobs, n, M, codebook, *P);
+  // the arrays keep the previous call's contents: this call's maps, and counters from zero
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(maps, P->maps, sizeof(CUtensorMap) * (size_t)n, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(counters, 0, sizeof(unsigned) * (size_t)(nlevels + 1), stream);
+  if (e == cudaSuccess) e = dispatch<kStepMaxGemvs, kStepMaxGemvs>(format, *P, counters, maps, true, stream);
+  delete P;
+  return e;
 }
 
 unsigned int read_clear_error_persist() { return read_clear_error_word_here(); }

@@ -572,38 +572,6 @@ __global__ void __launch_bounds__(kT5Threads, 1) w4_tc5_kernel(const __grid_cons
 
 // ---------------------------------------------------------------- host side
 
-using T5EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The driver's tensor-map encoder, looked up once through the runtime (no link against libcuda).
-static T5EncodeFn t5_encoder() {
-  static T5EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<T5EncodeFn>(f);
-  });
-  return fn;
-}
-
-// 2-D tiled map over a row-major [rows][cols] array with a 128-byte swizzle; zero fill outside.
-static bool t5_encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int es, const void* base, long long cols,
-                         long long rows, int box_cols, int box_rows) {
-  T5EncodeFn enc = t5_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)(cols * es)};
-  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Launch geometry of one GEMV on this kernel; host only, no device call.  False for shapes the
 // kernel does not take.
 bool plan_tc5(int M, int N, int K, int bs, int sms, Tc5Plan* o) {
@@ -654,7 +622,7 @@ static cudaError_t launch_tc5_nb(T5Params& p, const Tc5Plan& pl, bool pdl, cudaS
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  if (!t5_encode_2d(&p.tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.tm_x_base, p.K, p.M, kT5Kc, NB))
+  if (!encode_tmap_2d(&p.tm_x, 2, p.tm_x_base, p.K, p.M, kT5Kc, NB))
     return cudaErrorNotSupported;
   p.np = pl.np;
   p.stages = pl.ns;
@@ -687,7 +655,7 @@ cudaError_t launch_gemv_tc5(int format, const uint8_t* packed, const void* scale
       (reinterpret_cast<uintptr_t>(x) & 15))
     return cudaErrorNotSupported;
   T5Params p;
-  if (!t5_encode_2d(&p.tm_packed, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, packed, K / 2, N, kT5Sk / 2, kT5Rows))
+  if (!encode_tmap_2d(&p.tm_packed, 1, packed, K / 2, N, kT5Sk / 2, kT5Rows))
     return cudaErrorNotSupported;
   p.tm_x_base = x;
   p.scales = scales; p.codebook = codebook; p.y = y;

@@ -113,6 +113,10 @@ class DecodeStep:
         self.step = h
         return self
 
+    def counters(self):
+        """The level counters at the start of the step workspace (one per GEMV, plus one)."""
+        return self.workspace[: len(self.gemvs) + 1]
+
     def launch(self, stream=None):
         return w4.w4_step_launch(self.step, stream)
 
