@@ -271,18 +271,19 @@ int w4_gemv_sequence(const w4_gemv_desc* descs, int count, w4_stream_t stream) {
   return W4_OK;
 }
 
-// Step workspace: (count + 1) level counters, then, 64-byte aligned, one 128-byte TMA tensor map per
-// descriptor (written once by w4_step_create, read by every launch).
+// Step workspace: (count + 1) level counters, then, 128-byte aligned, the launch's device tables
+// (a TMA tensor map, a level and a GEMV descriptor per descriptor; written once by w4_step_create,
+// read by every launch).
 static size_t ws_counter_bytes(int count) { return ((size_t)(count + 1) * 4 + 15) & ~(size_t)15; }
 
-static CUtensorMap* ws_maps(void* workspace, int count) {
+static void* ws_tables(void* workspace, int count) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(workspace) + ws_counter_bytes(count);
-  return reinterpret_cast<CUtensorMap*>((a + 63) & ~(uintptr_t)63);
+  return reinterpret_cast<void*>((a + 127) & ~(uintptr_t)127);
 }
 
 int64_t w4_step_workspace_bytes(int count) {
-  if (count < 1) return 0;
-  return ((int64_t)ws_counter_bytes(count) + 64 + (int64_t)count * (int64_t)sizeof(CUtensorMap) + 255) / 256 * 256;
+  if (count < 1 || count > w4::kStepMaxGemvs) return count < 1 ? 0 : ((int64_t)(count + 1) * 4 + 255) / 256 * 256;
+  return ((int64_t)ws_counter_bytes(count) + 128 + (int64_t)w4::step_tables_bytes(count) + 255) / 256 * 256;
 }
 
 // True when the step can run as one persistent CUDA-core launch.
@@ -316,17 +317,17 @@ int w4_step_create(const w4_gemv_desc* descs, int count, void* workspace, w4_ste
       jobs[i] = w4::StepJob{d.packed, d.scales, reinterpret_cast<const __half*>(d.x), reinterpret_cast<__half*>(d.y),
                             d.N, d.K, d.blocksize, d.level};
     }
-    // counters zeroed, tensor maps written once, before the capture
-    std::vector<CUtensorMap> maps((size_t)count);
-    e = w4::step_simt_maps(descs[0].format, jobs.data(), count, descs[0].M, maps.data());
+    // counters zeroed, tables written once, before the capture
+    std::vector<uint8_t> blob(w4::step_tables_bytes(count));
+    e = w4::step_simt_tables(descs[0].format, jobs.data(), count, descs[0].M, ws_tables(workspace, count),
+                             blob.data());
     if (e == cudaErrorNotSupported) {
       cudaStreamDestroy(cs);
       return W4_ERR_UNSUPPORTED;
     }
     if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, (size_t)w4_step_workspace_bytes(count), cs);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(ws_maps(workspace, count), maps.data(), sizeof(CUtensorMap) * (size_t)count,
-                          cudaMemcpyHostToDevice, cs);
+      e = cudaMemcpyAsync(ws_tables(workspace, count), blob.data(), blob.size(), cudaMemcpyHostToDevice, cs);
     if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
     if (e != cudaSuccess) {
       cudaStreamDestroy(cs);
@@ -339,7 +340,7 @@ int w4_step_create(const w4_gemv_desc* descs, int count, void* workspace, w4_ste
   if (e == cudaSuccess) {
     if (persistent) {
       cudaError_t e3 = w4::launch_step_simt(descs[0].format, jobs.data(), count, descs[0].M, descs[0].codebook,
-                                            reinterpret_cast<unsigned*>(workspace), ws_maps(workspace, count), true, cs);
+                                            reinterpret_cast<unsigned*>(workspace), ws_tables(workspace, count), true, cs);
       if (e3 != cudaSuccess) s = (e3 == cudaErrorNotSupported) ? W4_ERR_UNSUPPORTED : cuda_status(e3);
     } else {
       for (int i = 0; i < count && s == W4_OK; ++i) {

@@ -73,8 +73,10 @@ unsigned int read_clear_error_tc5();
 // A whole decode step in one persistent launch of the batch 1 ... 8 kernel.  GEMVs are grouped into
 // levels (0, 1, ... non-decreasing along the array); a level reads its x only after every GEMV of
 // the previous level is complete.  counters: device memory of (number of levels + 1) words, zero
-// before the first launch; the kernel leaves it zero again.  maps: device memory holding the n
-// tensor maps step_simt_maps() returns for the same arguments (64-byte aligned, 128 bytes each).
+// before the first launch; the kernel leaves it zero again.  Tables: device memory of
+// step_tables_bytes(n) bytes, 128-byte aligned, holding what step_simt_tables() builds for the
+// same arguments and that base address (tensor maps, levels, GEMVs); written once, read by every
+// launch.
 constexpr int kStepMaxGemvs = 256;
 struct StepJob {
   const uint8_t* packed;
@@ -83,12 +85,13 @@ struct StepJob {
   __half* y;
   int N, K, bs, level;
 };
-cudaError_t step_simt_maps(int format, const StepJob* jobs, int n, int M, CUtensorMap* maps_out);
+size_t step_tables_bytes(int n);
+cudaError_t step_simt_tables(int format, const StepJob* jobs, int n, int M, const void* dev_base, void* blob);
 cudaError_t launch_step_simt(int format, const StepJob* jobs, int n, int M, const float* codebook, unsigned* counters,
-                             const CUtensorMap* maps, bool pdl, cudaStream_t stream);
+                             const void* dev_tables, bool pdl, cudaStream_t stream);
 
-// The same launch with the level counters and the tensor maps in fixed arrays inside the library (no
-// caller memory): the maps are copied in on `stream` before the launch.
+// The same launch with the level counters and the tables in fixed arrays inside the library (no
+// caller memory): the tables are copied in on `stream` before the launch.
 int noalloc_max_levels();
 cudaError_t launch_step_simt_noalloc(int format, const StepJob* jobs, int n, int M, const float* codebook,
                                      int nlevels, cudaStream_t stream);

@@ -229,76 +229,4 @@ __device__ __forceinline__ void mma_unit(float (&acc)[4], uint32_t a0, uint32_t 
   }
 }
 
-// The same unit split in two, so that the weights of a unit can be decoded before its x exists:
-// decode_unit turns the packed bytes of both rows into the A fragments of every MMA of the span and
-// loads the scales (FULL spans, NSC scales per row as one vector); mma_decoded loads x and runs the
-// MMAs.  Together they compute what mma_unit<KB, SC32, NSC> computes, in the same order.
-template <int KB>
-struct DecodedUnit {
-  uint32_t a[kSpanK / KB][KB / 16][4];
-  float sk0[kSpanK / KB], sk1[kSpanK / KB];
-};
-
-template <int KB, bool SC32, int NSC>
-__device__ __forceinline__ void decode_unit(DecodedUnit<KB>& du, uint32_t a0, uint32_t a1,
-                                            const uint32_t (&off0)[kSpanK / KB], const uint32_t (&off1)[kSpanK / KB],
-                                            uint32_t s0a, uint32_t s1a, bool v0, bool v1, uint32_t lut_lane) {
-  constexpr int NKB = kSpanK / KB;
-  constexpr int NMMA = KB / 16;
-#pragma unroll
-  for (int j = 0; j < NKB; ++j) {
-    uint32_t w0[2], w1[2];
-    if (KB == 64) {
-      const uint2 p = lds_ring64(a0 + off0[j]), q = lds_ring64(a1 + off1[j]);
-      w0[0] = p.x; w0[1] = p.y; w1[0] = q.x; w1[1] = q.y;
-    } else {
-      w0[0] = w0[1] = lds_ring32(a0 + off0[j]);
-      w1[0] = w1[1] = lds_ring32(a1 + off1[j]);
-    }
-#pragma unroll
-    for (int s = 0; s < NMMA; ++s) {
-      const uint32_t ww0 = w0[(2 * s) >> 2], ww1 = w1[(2 * s) >> 2];
-      const int b = (2 * s) & 3;
-      du.a[j][s][0] = lut_pair(lut_lane, ww0, b);
-      du.a[j][s][1] = lut_pair(lut_lane, ww1, b);
-      du.a[j][s][2] = lut_pair(lut_lane, ww0, b + 1);
-      du.a[j][s][3] = lut_pair(lut_lane, ww1, b + 1);
-    }
-  }
-  span_scales<KB, SC32, NSC>(du.sk0, s0a);
-  span_scales<KB, SC32, NSC>(du.sk1, s1a);
-#pragma unroll
-  for (int j = 0; j < NKB; ++j) {
-    if (!v0) du.sk0[j] = 0.0f;
-    if (!v1) du.sk1[j] = 0.0f;
-  }
-}
-
-template <int KB>
-__device__ __forceinline__ void mma_decoded(float (&acc)[4], const DecodedUnit<KB>& du, const uint8_t* xg,
-                                            bool xok) {
-  constexpr int NKB = kSpanK / KB;
-  constexpr int NMMA = KB / 16;
-  uint32_t xr[NKB][KB / 8];
-#pragma unroll
-  for (int j = 0; j < NKB; ++j) {
-#pragma unroll
-    for (int q = 0; q < KB / 32; ++q) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (xok) v = ld_x_v4(xg + j * (KB * 2) + 16 * q);
-      xr[j][4 * q + 0] = v.x; xr[j][4 * q + 1] = v.y; xr[j][4 * q + 2] = v.z; xr[j][4 * q + 3] = v.w;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < NKB; ++j) {
-    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int s = 0; s < NMMA; ++s) mma16816(d, du.a[j][s], xr[j][2 * s], xr[j][2 * s + 1]);
-    acc[0] = fmaf(du.sk0[j], d[0], acc[0]);
-    acc[1] = fmaf(du.sk0[j], d[1], acc[1]);
-    acc[2] = fmaf(du.sk1[j], d[2], acc[2]);
-    acc[3] = fmaf(du.sk1[j], d[3], acc[3]);
-  }
-}
-
 }  // namespace w4

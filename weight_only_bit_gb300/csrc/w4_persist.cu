@@ -49,7 +49,9 @@
 // Every wait is bounded in wall-clock time; a lost wait is recorded in the device error word and
 // the kernel runs to its end without further waiting.
 #include <cstdint>
+#include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -71,8 +73,6 @@ constexpr int kRedBufs = 2;            // partial-sum buffers: the reducer may l
 constexpr int kRedCapFloats = 12288;   // largest partial-sum buffer (floats)
 constexpr int kSmemCap = 227 * 1024;
 constexpr int kMaxRowsPerTile = 256;  // TMA box rows
-constexpr int kPrefetchTiles = 2;      // L2 prefetch distance, in the CTA's tiles
-constexpr bool kDecodeAhead = false;   // decode a warp's first unit of a level before that level's wait
 
 __host__ __device__ constexpr int span_count(int K) { return (K + kSpanK - 1) / kSpanK; }
 __host__ __device__ constexpr int box_count(int K) { return (K + kBoxK - 1) / kBoxK; }
@@ -96,23 +96,42 @@ struct PGemv {
   int tile0, ntiles, srb;  // global tile range; scale bytes per row
   int nspan, nbox, slot, cp;  // spans (128 k) and TMA boxes (256 k) per row; shared bytes per box;
                               // partial stride (floats)
+  int pad_[3];
 };
+static_assert(sizeof(PGemv) % 16 == 0, "PGemv is read as 16-byte vectors");
 
 struct PLevel {
   int gemv0, ngemv, tile0, ntiles;
 };
 
-template <int MAXL, int MAXG>
+// Launch parameters.  A single-GEMV launch carries its level, GEMV and tensor map here; a
+// multi-GEMV launch reads them from tables in device memory (written once by the host), because a
+// parameter block large enough for a decode step does not stay in the constant cache and every
+// tile would pay for that.
 struct PParams {
   CUtensorMap map1;        // the tensor map of a single-GEMV launch
   const float* codebook;   // NF4 code book (format 0)
   unsigned int* counters;  // [nlevels + 1] when nlevels > 1, else null
+  const PLevel* lvt;       // device tables of a multi-GEMV launch (null: lv1 and gm1)
+  const PGemv* gmt;
   int fmt;                 // 0 NF4 (FP32 absmax), 1 INT4 (FP16 scale), 2 FP4 E2M1 (FP16 scale)
   int nlevels, ngemvs, M, inject_timeout;
   int stages, stage_w, stage_s, red_floats;
-  PLevel lv[MAXL];
-  PGemv gm[MAXG];
+  PLevel lv1;
+  PGemv gm1;
 };
+
+template <class T>
+__device__ __forceinline__ T ldg_struct(const T* q) {
+  T v;
+  const uint4* src = reinterpret_cast<const uint4*>(q);
+  uint4* dst = reinterpret_cast<uint4*>(&v);
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(T) / 16); ++i) dst[i] = __ldg(src + i);
+  return v;
+}
+__device__ __forceinline__ PLevel level_at(const PParams& p, int L) { return p.lvt ? ldg_struct(p.lvt + L) : p.lv1; }
+__device__ __forceinline__ PGemv gemv_at(const PParams& p, int g) { return p.gmt ? ldg_struct(p.gmt + g) : p.gm1; }
 
 struct PLayout {
   int lut, w, s, red, bar, total;
@@ -183,15 +202,6 @@ __device__ __forceinline__ bool wait_gate(volatile int* gate, uint32_t site) {
   return false;
 }
 
-// Asks L2 to fetch [p, p + bytes) from DRAM (no data to the SM).  The range is trimmed inwards to
-// 16-byte boundaries, so nothing outside it is touched.
-__device__ __forceinline__ void prefetch_l2(const void* p, size_t bytes) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uintptr_t lo = (a + 15) & ~(uintptr_t)15, hi = (a + bytes) & ~(uintptr_t)15;
-  if (hi > lo)
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"((uint32_t)(hi - lo)) : "memory");
-}
-
 // 2-D TMA tensor copy global -> shared (box at coordinates c0 = byte column, c1 = row); completion
 // adds the box's bytes to `bar`.  dst: 1 KB aligned shared address.
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
@@ -204,42 +214,53 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
 }
 
 
-// The tiles of one CTA, in order across levels: level, GEMV and global tile index.
-template <int MAXL, int MAXG>
+// The tiles of one CTA, in order across levels: level, GEMV and global tile index (with the end
+// tiles of the current level and GEMV kept, so that a step reads the tables only when it moves on).
 struct TileCursor {
-  int L, g, t;
-  __device__ __forceinline__ void start(const PParams<MAXL, MAXG>& p) {
+  int L, g, t, lend, gend;
+  __device__ __forceinline__ void start(const PParams& p) {
     L = 0;
-    g = 0;
-    t = 0;
     seek(p);
   }
-  // from level L on: this CTA's first tile of the first level that has one
-  __device__ __forceinline__ void seek(const PParams<MAXL, MAXG>& p) {
-    while (L < p.nlevels) {
-      t = first_owned(p.lv[L].tile0);
-      if (t < p.lv[L].tile0 + p.lv[L].ntiles) break;
-      ++L;
-    }
-    if (L < p.nlevels) {
-      g = p.lv[L].gemv0;
-      while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
+  __device__ __forceinline__ void find_gemv(const PParams& p) {
+    for (;;) {
+      const PGemv gm = gemv_at(p, g);
+      gend = gm.tile0 + gm.ntiles;
+      if (t < gend) break;
+      ++g;
     }
   }
-  __device__ __forceinline__ bool valid(const PParams<MAXL, MAXG>& p) const { return L < p.nlevels; }
-  __device__ __forceinline__ void next(const PParams<MAXL, MAXG>& p) {
+  // from level L on: this CTA's first tile of the first level that has one
+  __device__ __forceinline__ void seek(const PParams& p) {
+    while (L < p.nlevels) {
+      const PLevel lv = level_at(p, L);
+      t = first_owned(lv.tile0);
+      lend = lv.tile0 + lv.ntiles;
+      if (t < lend) {
+        g = lv.gemv0;
+        find_gemv(p);
+        return;
+      }
+      ++L;
+    }
+  }
+  __device__ __forceinline__ bool valid(const PParams& p) const { return L < p.nlevels; }
+  __device__ __forceinline__ void next(const PParams& p) {
     t += (int)gridDim.x;
-    if (t >= p.lv[L].tile0 + p.lv[L].ntiles) {
+    if (t >= lend) {
       ++L;
       seek(p);
       return;
     }
-    while (t >= p.gm[g].tile0 + p.gm[g].ntiles) ++g;
+    if (t >= gend) {
+      ++g;
+      find_gemv(p);
+    }
   }
 };
 
-template <int KB, bool SC32, int MAXL, int MAXG>
-__global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid_constant__ PParams<MAXL, MAXG> p) {
+template <int KB, bool SC32>
+__global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid_constant__ PParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const PLayout Lo = playout(p.stages, p.stage_w, p.stage_s, p.red_floats);
@@ -274,26 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
     // ================================================================ producer warp
     if (p.inject_timeout) return;   // test hook: nothing issued, nothing in flight
     const uint64_t pol = policy_evict_first();
-    // L2 prefetch cursor, kPrefetchTiles ahead of the copies
-    TileCursor<MAXL, MAXG> pc;
-    pc.start(p);
-    auto prefetch_tile = [&](const TileCursor<MAXL, MAXG>& c) {
-      const PGemv& gm = p.gm[c.g];
-      const int r0 = (c.t - gm.tile0) * gm.rpt;
-      const int nrows = min(gm.rpt, gm.N - r0);
-      prefetch_l2(gm.packed + (size_t)r0 * (gm.K / 2), (size_t)nrows * (gm.K / 2));
-      prefetch_l2(reinterpret_cast<const uint8_t*>(gm.scales) + (size_t)r0 * gm.srb, (size_t)nrows * gm.srb);
-    };
-    if (lane == 0) {
-      for (int i = 0; i < kPrefetchTiles && pc.valid(p); ++i, pc.next(p)) prefetch_tile(pc);
-    }
-    TileCursor<MAXL, MAXG> cur;
+    TileCursor cur;
     cur.start(p);
     int j = 0;
     int prev_level = -1;
     bool ok = true;
     for (; cur.valid(p); cur.next(p), ++j) {
-      const PGemv& gm = p.gm[cur.g];
+      const PGemv gm = gemv_at(p, cur.g);
       const int st = j % NS;
       const int round = j / NS;
       // Copies of the first NS tiles may overlap the previous kernel in the stream; the bounded
@@ -322,10 +330,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
           for (uint32_t b = sbulk; b < sbytes; ++b) dst_s[b] = src_s[b];   // sub-16-byte tail
           // every box carries rpt rows (zeros past the matrix)
           mbar_arrive_expect_tx(&full[st], (uint32_t)gm.nbox * (uint32_t)gm.rpt * 128u + sbulk);
-          if (pc.valid(p)) {
-            prefetch_tile(pc);
-            pc.next(p);
-          }
         } else {
           mbar_arrive(&full[st]);
         }
@@ -350,13 +354,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
   if (warp == kConsumerWarps + 1) {
     // ================================================================ reducer warp
     pdl_wait();   // counters are touched only after the previous kernel in the stream completed
-    TileCursor<MAXL, MAXG> cur;
+    TileCursor cur;
     cur.start(p);
     int j = 0;
     bool ok = true;
     for (; cur.valid(p); ++j) {
       const int L = cur.L;
-      const PGemv gm = p.gm[cur.g];
+      const PGemv gm = gemv_at(p, cur.g);
       const int t = cur.t;
       const int b = j % kRedBufs;
       if (ok) ok = mbar_wait(&rfull[b], (j / kRedBufs) & 1, 0x203);
@@ -416,12 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
   int ubase = 0;            // units of this CTA's earlier tiles (round-robin continues across tiles)
   bool ok = true;
   bool pdl_done = false;
-  TileCursor<MAXL, MAXG> cur;
+  TileCursor cur;
   cur.start(p);
   int Lcur = -1;
   for (; cur.valid(p); cur.next(p), ++j) {
     const int L = cur.L;
-    const PGemv gm = p.gm[cur.g];
+    const PGemv gm = gemv_at(p, cur.g);
     const int st = j % NS;
     const int b = j % kRedBufs;
     const int r0 = (cur.t - gm.tile0) * gm.rpt;
@@ -441,48 +445,23 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
     const int u0 = (warp - ubase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
     int rg = u0 / gm.nspan, c = u0 - rg * gm.nspan;
     const int rsub_a = KB == 64 ? 2 * g : g, rsub_b = rsub_a + (KB == 64 ? 1 : 8);
-    bool first_done = false;
     bool is_level_end;
     {
-      TileCursor<MAXL, MAXG> nx = cur;
+      TileCursor nx = cur;
       nx.next(p);
       is_level_end = nx.L != L && nx.L < p.nlevels;
     }
     if (L != Lcur) {
-      // ---- this CTA's first tile of the level: decode this warp's first unit of it before the
-      // wait for the previous level (weights never depend on it), wait, then multiply it by x
-      DecodedUnit<KB> du;
-      bool pre = false;
+      // ---- this CTA's first tile of the level: its weights are in (the producer never holds the
+      // first tile of a level back), then wait until this level's inputs exist
       if (ok) ok = mbar_wait(&full[st], (j / NS) & 1, 0x205);
-      if (kDecodeAhead && ok && full_last && u0 < units) {
-        const int ra = rg * 16 + rsub_a, rb = rg * 16 + rsub_b;
-        const uint32_t so = (uint32_t)(((c * kSpanK) >> lgbs) * (SC32 ? 4 : 2));
-        const uint32_t hm = (uint32_t)(c & 1) << 6;
-        uint32_t o0[NKB], o1[NKB];
-#pragma unroll
-        for (int jj = 0; jj < NKB; ++jj) { o0[jj] = off0[jj] ^ hm; o1[jj] = off1[jj] ^ hm; }
-        const uint32_t a0 = tile_s + (uint32_t)((c >> 1) * gm.slot + ra * 128), a1 = tile_s + (uint32_t)((c >> 1) * gm.slot + rb * 128);
-        const uint32_t s0a = stile_s + (uint32_t)(min(ra, nrows - 1) * gm.srb) + so;
-        const uint32_t s1a = stile_s + (uint32_t)(min(rb, nrows - 1) * gm.srb) + so;
-        const bool v0 = ra < nrows, v1 = rb < nrows;
-        pre = true;
-        if (KB == 32) {
-          if (lgbs == 5) decode_unit<KB, SC32, 4>(du, a0, a1, o0, o1, s0a, s1a, v0, v1, lut_lane);
-          else pre = false;
-        } else if (lgbs == 6) {
-          decode_unit<KB, SC32, 2>(du, a0, a1, o0, o1, s0a, s1a, v0, v1, lut_lane);
-        } else {
-          decode_unit<KB, SC32, 1>(du, a0, a1, o0, o1, s0a, s1a, v0, v1, lut_lane);
-        }
-      }
-      // ---- wait until this level's inputs exist
       if (!pdl_done) {
         pdl_wait();
         pdl_done = true;
       }
       if (L > 0 && p.counters) {
         // every CTA that owns a tile of level L-1 adds one when it has finished them all
-        const unsigned owners = (unsigned)min(G, p.lv[L - 1].ntiles);
+        const unsigned owners = (unsigned)min(G, level_at(p, L - 1).ntiles);
         if (tid == 0 && ok) ok = wait_counter(&p.counters[L - 1], owners, 0x204);
       }
       // the level's start for all consumers: thread 0's acquire orders every consumer's reads of
@@ -490,39 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
       asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");
       if (tid == 0) *gate = 1;
       Lcur = L;
-      if (pre) {
-        if (j >= kRedBufs && ok) ok = mbar_wait(&rfree[b], ((j / kRedBufs) - 1) & 1, 0x206);
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        mma_decoded<KB>(acc, du, xrow + c * (kSpanK * 2), xok);
-        if (ok) {
-          const int ra = rg * 16 + rsub_a, rb = rg * 16 + rsub_b;
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int m = 2 * tq + q;
-            if (m < p.M) {
-              if (ra < nrows) red[(m * nrows + ra) * gm.cp + c] = acc[q];
-              if (rb < nrows) red[(m * nrows + rb) * gm.cp + c] = acc[2 + q];
-            }
-          }
-        }
-        first_done = true;
-      }
     }
     // every lane waits for itself: one instruction per warp, no broadcast round trip
     if (ok) ok = mbar_wait(&full[st], (j / NS) & 1, 0x205);
     if (j >= kRedBufs && ok) ok = mbar_wait(&rfree[b], ((j / kRedBufs) - 1) & 1, 0x206);
     if (ok) {
       const int sshift = 31 - __clz(gm.bs / KB);
-      int u = u0;
-      if (first_done) {
-        u += kConsumerWarps;
-        c += kConsumerWarps;
-        while (c >= gm.nspan) {
-          c -= gm.nspan;
-          ++rg;
-        }
-      }
-      for (; u < units; u += kConsumerWarps) {
+      for (int u = u0; u < units; u += kConsumerWarps) {
         const int ra = rg * 16 + rsub_a, rb = rg * 16 + rsub_b;
         const int rac = min(ra, nrows - 1), rbc = min(rb, nrows - 1);
         const uint32_t a0 = tile_s + (uint32_t)((c >> 1) * gm.slot + ra * 128);
@@ -705,31 +658,33 @@ bool plan_simt(int format, int M, int K, int bs, SimtPlan* out) {
   return true;
 }
 
-// Everything a launch needs, computed on the host: parameters (levels, GEMVs and their tiling), the
-// tensor map of each GEMV (box rows = its rows per tile), and the geometry.
-template <int MAXL, int MAXG>
+// Everything a launch needs, computed on the host: parameters, the levels and GEMVs with their
+// tiling, the tensor map of each GEMV (box rows = its rows per tile), and the geometry.
 struct Prepared {
-  PParams<MAXL, MAXG> p;
-  CUtensorMap maps[MAXG];
+  PParams p;
+  std::vector<PLevel> lv;
+  std::vector<PGemv> gm;
+  std::vector<CUtensorMap> maps;
   Plan plan;
   int grid;
 };
 
-template <int MAXL, int MAXG>
-static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* codebook, Prepared<MAXL, MAXG>& P) {
+static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* codebook, Prepared& P) {
   int nlev = 0;
   for (int i = 0; i < n; ++i) nlev = max(nlev, jobs[i].level + 1);
-  if (n < 1 || n > MAXG || nlev > MAXL) return cudaErrorNotSupported;
+  if (n < 1 || n > kStepMaxGemvs || nlev > n) return cudaErrorNotSupported;
   if (!plan_layout(fmt, M, jobs, n, P.plan)) return cudaErrorNotSupported;
   const int gmax = device_sm_count();   // one CTA per SM: the ring is sized for the whole SM
-  PParams<MAXL, MAXG>& p = P.p;
+  P.lv.assign((size_t)nlev, PLevel{});
+  P.gm.assign((size_t)n, PGemv{});
+  P.maps.assign((size_t)n, CUtensorMap{});
+  PParams& p = P.p;
+  p = PParams{};
   p.codebook = codebook;
-  p.counters = nullptr;
   p.fmt = fmt;
   p.nlevels = nlev;
   p.ngemvs = n;
   p.M = M;
-  p.inject_timeout = 0;
   p.stages = P.plan.stages; p.stage_w = P.plan.stage_w; p.stage_s = P.plan.stage_s;
   p.red_floats = P.plan.red_floats;
   // tiling, level by level: balanced tiles per CTA, rows per tile within each GEMV's stage budget
@@ -745,9 +700,10 @@ static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* 
       rmin = min(rmin, gg.rpt_max);
       ++i;
     }
-    p.lv[Lv].gemv0 = first;
-    p.lv[Lv].ngemv = i - first;
-    p.lv[Lv].tile0 = tile;
+    PLevel& lv = P.lv[(size_t)Lv];
+    lv.gemv0 = first;
+    lv.ngemv = i - first;
+    lv.tile0 = tile;
     const long long tpc = (rows + (long long)gmax * rmin - 1) / ((long long)gmax * rmin);
     for (int q = first; q < i; ++q) {
       GeomG gg;
@@ -756,20 +712,22 @@ static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* 
       if (rpt > 16) rpt = (rpt + 15) & ~15;                          // whole MMA row groups
       rpt = ((rpt + gg.align_rows - 1) / gg.align_rows) * gg.align_rows;
       rpt = min(rpt, gg.rpt_max);
-      PGemv& g = p.gm[q];
+      PGemv& g = P.gm[(size_t)q];
       g.packed = jobs[q].packed; g.scales = jobs[q].scales; g.x = jobs[q].x; g.y = jobs[q].y;
       g.tmap = nullptr;
       g.N = jobs[q].N; g.K = jobs[q].K; g.bs = jobs[q].bs; g.rpt = rpt;
       g.tile0 = tile; g.ntiles = (g.N + rpt - 1) / rpt; g.srb = gg.srb;
       g.nspan = gg.nspan; g.nbox = gg.nbox; g.slot = span_slot(rpt); g.cp = gg.cp;
-      if (!encode_tmap_2d(&P.maps[q], 1, g.packed, g.K / 2, g.N, kBoxK / 2, rpt)) return cudaErrorNotSupported;
+      if (!encode_tmap_2d(&P.maps[(size_t)q], 1, g.packed, g.K / 2, g.N, kBoxK / 2, rpt)) return cudaErrorNotSupported;
       tile += g.ntiles;
     }
-    p.lv[Lv].ntiles = tile - p.lv[Lv].tile0;
-    max_level_tiles = max(max_level_tiles, p.lv[Lv].ntiles);
+    lv.ntiles = tile - lv.tile0;
+    max_level_tiles = max(max_level_tiles, lv.ntiles);
   }
   P.grid = nlev > 1 ? gmax : min(gmax, max_level_tiles);
   p.map1 = P.maps[0];
+  p.lv1 = P.lv[0];
+  p.gm1 = P.gm[0];
   return cudaSuccess;
 }
 
@@ -779,11 +737,9 @@ struct KernelSetup {
   bool attr_done[kMaxDevices] = {};
 };
 
-// maps: device array of the n tensor maps (multi-GEMV launches) or null (single GEMV: map1).
-template <int KB, bool SC32, int MAXL, int MAXG>
-static cudaError_t launch_prepared(Prepared<MAXL, MAXG>& P, unsigned* counters, const CUtensorMap* maps, bool pdl,
-                                   cudaStream_t stream) {
-  auto kern = w4_persistent_kernel<KB, SC32, MAXL, MAXG>;
+template <int KB, bool SC32>
+static cudaError_t launch_prepared(Prepared& P, unsigned* counters, bool pdl, cudaStream_t stream) {
+  auto kern = w4_persistent_kernel<KB, SC32>;
   static KernelSetup setup;   // one per instance
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
@@ -795,11 +751,10 @@ static cudaError_t launch_prepared(Prepared<MAXL, MAXG>& P, unsigned* counters, 
       setup.attr_done[dev] = true;
     }
   }
-  PParams<MAXL, MAXG>& p = P.p;
+  PParams& p = P.p;
   if (p.nlevels > 1 && !counters) return cudaErrorInvalidValue;
-  if (p.ngemvs > 1 && !maps) return cudaErrorInvalidValue;
+  if (p.ngemvs > 1 && (!p.lvt || !p.gmt)) return cudaErrorInvalidValue;
   p.counters = p.nlevels > 1 ? counters : nullptr;
-  for (int q = 0; q < p.ngemvs; ++q) p.gm[q].tmap = p.ngemvs > 1 ? maps + q : nullptr;
   p.inject_timeout = take_fault_injection();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)P.grid);
@@ -816,16 +771,14 @@ static cudaError_t launch_prepared(Prepared<MAXL, MAXG>& P, unsigned* counters, 
   return e;
 }
 
-template <int MAXL, int MAXG>
-static cudaError_t dispatch(int fmt, Prepared<MAXL, MAXG>& P, unsigned* counters, const CUtensorMap* maps, bool pdl,
-                            cudaStream_t s) {
+static cudaError_t dispatch(int fmt, Prepared& P, unsigned* counters, bool pdl, cudaStream_t s) {
   const bool kb64 = P.plan.kb == 64;
   if (fmt == 0) {
-    if (kb64) return launch_prepared<64, true, MAXL, MAXG>(P, counters, maps, pdl, s);
-    return launch_prepared<32, true, MAXL, MAXG>(P, counters, maps, pdl, s);
+    if (kb64) return launch_prepared<64, true>(P, counters, pdl, s);
+    return launch_prepared<32, true>(P, counters, pdl, s);
   }
-  if (kb64) return launch_prepared<64, false, MAXL, MAXG>(P, counters, maps, pdl, s);
-  return launch_prepared<32, false, MAXL, MAXG>(P, counters, maps, pdl, s);
+  if (kb64) return launch_prepared<64, false>(P, counters, pdl, s);
+  return launch_prepared<32, false>(P, counters, pdl, s);
 }
 
 cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scales, const float* codebook,
@@ -833,68 +786,81 @@ cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scal
                              cudaStream_t stream) {
   if (M < 1 || M > 8) return cudaErrorNotSupported;
   Job jb{packed, scales, x, y, N, K, bs, 0};
-  Prepared<1, 1> P;
-  cudaError_t e = prepare<1, 1>(format, &jb, 1, M, codebook, P);
+  Prepared P;
+  cudaError_t e = prepare(format, &jb, 1, M, codebook, P);
   if (e != cudaSuccess) return e;
-  return dispatch<1, 1>(format, P, nullptr, nullptr, pdl, stream);
+  return dispatch(format, P, nullptr, pdl, stream);
 }
 
-using StepPrepared = Prepared<kStepMaxGemvs, kStepMaxGemvs>;
+// Device tables of a multi-GEMV launch, at a 128-byte aligned base: the n tensor maps (128 bytes
+// each), the levels (16 bytes each, at most n of them, padded to 128 bytes), the GEMVs.
+static size_t tables_levels_off(int n) { return (size_t)n * sizeof(CUtensorMap); }
+static size_t tables_gemvs_off(int n) { return tables_levels_off(n) + (((size_t)n * sizeof(PLevel) + 127) & ~(size_t)127); }
+size_t step_tables_bytes(int n) { return tables_gemvs_off(n) + (size_t)n * sizeof(PGemv); }
 
-static cudaError_t prepare_step(int format, const StepJob* jobs, int n, int M, const float* codebook, StepPrepared& P) {
+static cudaError_t prepare_step(int format, const StepJob* jobs, int n, int M, const float* codebook, Prepared& P) {
   if (M < 1 || M > 8 || n < 1 || n > kStepMaxGemvs) return cudaErrorNotSupported;
-  Job js[kStepMaxGemvs];
+  std::vector<Job> js((size_t)n);
   for (int i = 0; i < n; ++i) {
-    js[i] = Job{jobs[i].packed, jobs[i].scales, jobs[i].x, jobs[i].y, jobs[i].N, jobs[i].K, jobs[i].bs, jobs[i].level};
+    js[(size_t)i] = Job{jobs[i].packed, jobs[i].scales, jobs[i].x, jobs[i].y, jobs[i].N, jobs[i].K, jobs[i].bs,
+                        jobs[i].level};
   }
-  return prepare<kStepMaxGemvs, kStepMaxGemvs>(format, js, n, M, codebook, P);
+  return prepare(format, js.data(), n, M, codebook, P);
 }
 
-cudaError_t step_simt_maps(int format, const StepJob* jobs, int n, int M, CUtensorMap* maps_out) {
-  StepPrepared* P = new StepPrepared();   // large: build on the heap
-  cudaError_t e = prepare_step(format, jobs, n, M, nullptr, *P);
-  if (e == cudaSuccess)
-    for (int i = 0; i < n; ++i) maps_out[i] = P->maps[i];
-  delete P;
-  return e;
+cudaError_t step_simt_tables(int format, const StepJob* jobs, int n, int M, const void* dev_base, void* blob) {
+  Prepared P;
+  cudaError_t e = prepare_step(format, jobs, n, M, nullptr, P);
+  if (e != cudaSuccess) return e;
+  uint8_t* out = static_cast<uint8_t*>(blob);
+  memset(out, 0, step_tables_bytes(n));
+  const uintptr_t base = reinterpret_cast<uintptr_t>(dev_base);
+  for (int q = 0; q < n; ++q) P.gm[(size_t)q].tmap = reinterpret_cast<const CUtensorMap*>(base + (size_t)q * sizeof(CUtensorMap));
+  memcpy(out, P.maps.data(), (size_t)n * sizeof(CUtensorMap));
+  memcpy(out + tables_levels_off(n), P.lv.data(), P.lv.size() * sizeof(PLevel));
+  memcpy(out + tables_gemvs_off(n), P.gm.data(), (size_t)n * sizeof(PGemv));
+  return cudaSuccess;
 }
 
 cudaError_t launch_step_simt(int format, const StepJob* jobs, int n, int M, const float* codebook, unsigned* counters,
-                             const CUtensorMap* maps, bool pdl, cudaStream_t stream) {
-  StepPrepared* P = new StepPrepared();
-  cudaError_t e = prepare_step(format, jobs, n, M, codebook, *P);
-  if (e == cudaSuccess) e = dispatch<kStepMaxGemvs, kStepMaxGemvs>(format, *P, counters, maps, pdl, stream);
-  delete P;
-  return e;
+                             const void* dev_tables, bool pdl, cudaStream_t stream) {
+  Prepared P;
+  cudaError_t e = prepare_step(format, jobs, n, M, codebook, P);
+  if (e != cudaSuccess) return e;
+  const uint8_t* base = static_cast<const uint8_t*>(dev_tables);
+  P.p.lvt = reinterpret_cast<const PLevel*>(base + tables_levels_off(n));
+  P.p.gmt = reinterpret_cast<const PGemv*>(base + tables_gemvs_off(n));
+  return dispatch(format, P, counters, pdl, stream);
 }
 
 // ---------------------------------------------------------------------------------------------
-// Counters and tensor maps for w4_gemv_levels_noalloc: fixed arrays inside the library, for callers
-// that cannot allocate device memory.  In host code the names are only stand-ins for the device
+// Counters and tables for w4_gemv_levels_noalloc: fixed arrays inside the library, for callers that
+// cannot allocate device memory.  In host code the names are only stand-ins for the device
 // objects; their device addresses are looked up once per device and cached.
 constexpr int kNoAllocMaxLevels = 256;
+constexpr size_t kNoAllocTableBytes = (size_t)kStepMaxGemvs * (sizeof(CUtensorMap) + sizeof(PLevel) + sizeof(PGemv));
 static __device__ __align__(256) unsigned int g_noalloc_counters[kNoAllocMaxLevels + 1];
-static __device__ __align__(128) CUtensorMap g_noalloc_maps[kStepMaxGemvs];
+static __device__ __align__(128) uint4 g_noalloc_tables[kNoAllocTableBytes / 16];
 
-static cudaError_t noalloc_arrays(unsigned** counters, CUtensorMap** maps) {
+static cudaError_t noalloc_arrays(unsigned** counters, void** tables) {
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
   static std::mutex mu;
   static unsigned* caddr[kMaxDevices] = {};
-  static CUtensorMap* maddr[kMaxDevices] = {};
+  static void* taddr[kMaxDevices] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (caddr[dev] == nullptr) {
     void* pc = nullptr;
-    void* pm = nullptr;
+    void* pt = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&pc, g_noalloc_counters);   // with this device current
     if (e != cudaSuccess) return e;
-    e = cudaGetSymbolAddress(&pm, g_noalloc_maps);
+    e = cudaGetSymbolAddress(&pt, g_noalloc_tables);
     if (e != cudaSuccess) return e;
     caddr[dev] = static_cast<unsigned*>(pc);
-    maddr[dev] = static_cast<CUtensorMap*>(pm);
+    taddr[dev] = pt;
   }
   *counters = caddr[dev];
-  *maps = maddr[dev];
+  *tables = taddr[dev];
   return cudaSuccess;
 }
 
@@ -903,18 +869,18 @@ int noalloc_max_levels() { return kNoAllocMaxLevels; }
 cudaError_t launch_step_simt_noalloc(int format, const StepJob* jobs, int n, int M, const float* codebook,
                                      int nlevels, cudaStream_t stream) {
   if (nlevels < 1 || nlevels > kNoAllocMaxLevels || n > kStepMaxGemvs) return cudaErrorInvalidValue;
+  static_assert(kNoAllocTableBytes >= kStepMaxGemvs * sizeof(CUtensorMap) + kStepMaxGemvs * sizeof(PLevel) +
+                                          kStepMaxGemvs * sizeof(PGemv), "no-alloc table array too small");
   unsigned* counters = nullptr;
-  CUtensorMap* maps = nullptr;
-  cudaError_t e = noalloc_arrays(&counters, &maps);
+  void* tables = nullptr;
+  cudaError_t e = noalloc_arrays(&counters, &tables);
   if (e != cudaSuccess) return e;
-  StepPrepared* P = new StepPrepared();
-  e = prepare_step(format, jobs, n, M, codebook, *P);
-  // the arrays keep the previous call's contents: this call's maps, and counters from zero
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(maps, P->maps, sizeof(CUtensorMap) * (size_t)n, cudaMemcpyHostToDevice, stream);
+  // the arrays keep the previous call's contents: this call's tables, and counters from zero
+  std::vector<uint8_t> blob(step_tables_bytes(n));
+  e = step_simt_tables(format, jobs, n, M, tables, blob.data());
+  if (e == cudaSuccess) e = cudaMemcpyAsync(tables, blob.data(), blob.size(), cudaMemcpyHostToDevice, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(counters, 0, sizeof(unsigned) * (size_t)(nlevels + 1), stream);
-  if (e == cudaSuccess) e = dispatch<kStepMaxGemvs, kStepMaxGemvs>(format, *P, counters, maps, true, stream);
-  delete P;
+  if (e == cudaSuccess) e = launch_step_simt(format, jobs, n, M, codebook, counters, tables, true, stream);
   return e;
 }
 
