@@ -39,6 +39,20 @@ Readings where the pages are silent (each is pinned by tests/test_oracle_pins.py
   * INT4 nibble order: the same as NF4 (element 2j in the high nibble).
   * Dequantised INT4 weight: (q - 8) * s, exact in FP32.
   * GEMV reference: y[m][n] = sum_k w_hat[n][k] * x[m][k] in float64.
+
+  FP4 (E2M1) -- "LLM Compressor 0.14: GPTQ's 15x speedup is one fused loop",
+  section "Details worth knowing": values rounded onto the grid
+  {0, 0.5, 1, 1.5, 2, 3, 4, 6} through a ladder of thresholds, the comparison
+  alternating between "<=" and "<" so that a value on a threshold goes to the
+  even code.  Readings where the page is silent:
+  * thresholds: the midpoints between consecutive grid values;
+  * code: sign bit (bit 3) set iff w < 0, the grid index in bits 0-2 (the E2M1
+    bit layout: exponent bits 1-2, mantissa bit 0); |value| above 6 stays at 6;
+  * scale: one FP16 scale per group of `group` weights along a row (32 unless
+    given), s = fl16(absmax / 6), the largest grid value; r = fl32(w / s);
+    s == 0 gives code 0 for the whole group;
+  * packing and dequantisation as for INT4: element 2j in the high nibble,
+    w_hat = value * s, exact in FP32.
 """
 from __future__ import annotations
 
@@ -51,6 +65,7 @@ __all__ = [
     "quantize_nf4", "dequantize_nf4", "quantize_int4", "dequantize_int4",
     "dequantize_nf4_rows", "dequantize_int4_rows", "gemv", "gemv_rows",
     "gemv_nf4", "gemv_int4",
+    "fp4_grid", "quantize_fp4", "dequantize_fp4", "dequantize_fp4_rows", "gemv_fp4",
 ]
 
 
@@ -167,6 +182,63 @@ def dequantize_int4_rows(packed, scale, rows, group: int = 128):
     return dequantize_int4(packed[rows], scale[rows], group)
 
 
+# --------------------------------------------------------------------------- FP4 (E2M1)
+def fp4_grid() -> np.ndarray:
+    """The eight E2M1 magnitudes, index 0 ... 7 (float64, all exact)."""
+    return np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+
+
+def _fp4_ladder(m: np.ndarray) -> np.ndarray:
+    """Grid index of magnitudes m >= 0: one rung per midpoint t_i between grid
+    values i and i + 1.  At an even i the value moves up only when m > t_i (a tie
+    stays on i), at an odd i when m >= t_i (a tie moves on to i + 1): either way
+    a tie lands on the even index.  Past the last rung the index stays 7."""
+    g = fp4_grid()
+    idx = np.zeros(m.shape, dtype=np.int64)
+    for i in range(7):
+        t = (g[i] + g[i + 1]) / 2.0
+        idx += (m > t) if i % 2 == 0 else (m >= t)
+    return idx
+
+
+def quantize_fp4(w: np.ndarray, group: int = 32):
+    """Group-wise FP4 (E2M1) with an FP16 scale per group.
+
+    Returns (packed uint8 [N, K/2], scale float16 [N, K/group]).
+    s = fl16(absmax / 6); r = fl32(w / s) (s == 0 -> r = 0); code =
+    (w < 0) << 3 | ladder(|r|).
+    """
+    w = np.asarray(w, dtype=np.float32)
+    n_rows, k = w.shape
+    assert k % group == 0
+    blocks = w.reshape(n_rows, k // group, group)
+    a = np.abs(blocks).max(axis=2).astype(np.float64)
+    # float64 quotient then FP16: innocuous double rounding (53 >= 2*11 + 2)
+    s16 = (a / 6.0).astype(np.float16)
+    s = s16.astype(np.float64)[..., None]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        r = np.where(s > 0.0, blocks.astype(np.float64) / s, 0.0).astype(np.float32)
+    mag = _fp4_ladder(np.abs(r.astype(np.float64)))
+    sign = (blocks < 0).astype(np.int64)
+    q = (sign << 3) | mag
+    return pack(q.reshape(n_rows, k).astype(np.uint8)), s16
+
+
+def dequantize_fp4(packed: np.ndarray, scale: np.ndarray, group: int = 32) -> np.ndarray:
+    """w_hat = (-1)^(bit 3) * grid[q & 7] * s, exact in FP32."""
+    q = unpack(packed).astype(np.int64)
+    n_rows, k = q.shape
+    v = fp4_grid()[q & 7] * np.where(q & 8, -1.0, 1.0)
+    s = np.repeat(np.asarray(scale, dtype=np.float16).astype(np.float64), group, axis=1)
+    assert s.shape == (n_rows, k)
+    return (v * s).astype(np.float32)
+
+
+def dequantize_fp4_rows(packed, scale, rows, group: int = 32):
+    rows = np.asarray(rows, dtype=np.int64)
+    return dequantize_fp4(packed[rows], scale[rows], group)
+
+
 # --------------------------------------------------------------------------- GEMV
 def gemv(w_hat: np.ndarray, x: np.ndarray) -> np.ndarray:
     """y[m][n] = sum_k w_hat[n][k] * x[m][k], in float64 (inputs are exact in float64)."""
@@ -190,3 +262,9 @@ def gemv_int4(packed, scale, x, group: int = 128, rows=None):
     if rows is None:
         return gemv(dequantize_int4(packed, scale, group), x)
     return gemv(dequantize_int4_rows(packed, scale, rows, group), x)
+
+
+def gemv_fp4(packed, scale, x, group: int = 32, rows=None):
+    if rows is None:
+        return gemv(dequantize_fp4(packed, scale, group), x)
+    return gemv(dequantize_fp4_rows(packed, scale, rows, group), x)
