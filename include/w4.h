@@ -10,12 +10,16 @@
  *         the +8 zero point; group size 128 as in "LLM Compressor 0.14: GPTQ's 15x speedup is
  *         one fused loop", section "How the 15x and 30x were measured"): groups of `group`
  *         weights of one row share one FP16 scale = absmax / 7; the nibble holds q + 8.
+ *   FP4  (E2M1: "LLM Compressor 0.14: GPTQ's 15x speedup is one fused loop", section "Details
+ *         worth knowing": the grid {0, 0.5, 1, 1.5, 2, 3, 4, 6} and its threshold ladder, ties
+ *         to the even code): groups of `group` (default 32) weights of one row share one FP16
+ *         scale = absmax / 6; the nibble holds the sign in bit 3 and the grid index in bits 0-2.
  *
  * Layouts (row-major, "out x in" = N x K, as the fused kernel of the first page indexes them,
  * section "Kernel Implementation")
  *   packed  uint8  [N][K/2]   byte j of a row = (code of element 2j) << 4 | code of element 2j+1
  *   absmax  float  [N][K/blocksize]            (NF4)
- *   scale   fp16   [N][K/group]                (INT4; IEEE binary16 bits in uint16_t)
+ *   scale   fp16   [N][K/group]                (INT4, FP4; IEEE binary16 bits in uint16_t)
  *   codebook float [16], ascending             (NF4)
  *   x       fp16   [M][K]   activations, M = batch (1 ... 128)
  *   y       fp16   [M][N]   y[m][n] = sum_k w_hat[n][k] * x[m][k], accumulated in FP32
@@ -64,11 +68,11 @@ typedef enum {
   W4_ERR_LIMIT = -8        /* beyond the fixed size of w4_gemv_levels_noalloc's counter array */
 } w4_status;
 
-typedef enum { W4_FMT_NF4 = 0, W4_FMT_INT4 = 1 } w4_format;
+typedef enum { W4_FMT_NF4 = 0, W4_FMT_INT4 = 1, W4_FMT_FP4 = 2 } w4_format;
 
 /* Limits of this build. */
 #define W4_MAX_BATCH 4096       /* M; above 128, batch tiles of 128 rows (prefill-sized)       */
-#define W4_MAX_K 10240          /* K; one consumer thread per 32-weight chunk of a row         */
+#define W4_MAX_K 10240          /* K; sizes the batch 1 ... 8 kernel's partial-sum buffers     */
 
 /* ---------------------------------------------------------------------------------------
  * w4_nf4_codebook -- the 16 NF4 code values, ascending, FP32 (host function, no CUDA).
@@ -103,6 +107,16 @@ int w4_quantize_nf4(const float* W, uint8_t* packed, float* absmax, const float*
 int w4_quantize_int4(const float* W, uint8_t* packed, uint16_t* scale,
                      int N, int K, int group, w4_stream_t stream);
 
+/* w4_quantize_fp4 -- group-wise FP4 (E2M1) with an FP16 scale ("LLM Compressor 0.14",
+ * section "Details worth knowing").  Per group: s = fp16(absmax / 6) (the FP32 quotient rounded
+ * to FP16); r = w / s (IEEE FP32 division); the grid index of |r| is found by a ladder over the
+ * midpoints t of consecutive grid values, moving up past an even rung when |r| > t and past an
+ * odd rung when |r| >= t, so that a value on a midpoint goes to the even index; |r| above 6
+ * stays at index 7; code = (w < 0) << 3 | index.  s == 0 gives code 0 for the whole group.
+ * |w| must stay below 6 * 65504. */
+int w4_quantize_fp4(const float* W, uint8_t* packed, uint16_t* scale,
+                    int N, int K, int group, w4_stream_t stream);
+
 /* w4_dequantize_nf4 -- W_out[n][k] = code[q] * absmax (FP32 product), a test and
  * debugging aid; the GEMVs never materialise this matrix.  W_out 8-byte aligned. */
 int w4_dequantize_nf4(const uint8_t* packed, const float* absmax, const float* codebook,
@@ -112,21 +126,34 @@ int w4_dequantize_nf4(const uint8_t* packed, const float* absmax, const float* c
 int w4_dequantize_int4(const uint8_t* packed, const uint16_t* scale, float* W_out,
                        int N, int K, int group, w4_stream_t stream);
 
+/* w4_dequantize_fp4 -- W_out[n][k] = (-1)^(bit 3) * grid[q & 7] * s, exact in FP32. */
+int w4_dequantize_fp4(const uint8_t* packed, const uint16_t* scale, float* W_out,
+                      int N, int K, int group, w4_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
- * w4_gemv_nf4 / w4_gemv_int4 -- y = x . dequant(W)^T in one pass: packed weights and scales
+ * w4_gemv_nf4 / w4_gemv_int4 / w4_gemv_fp4 -- y = x . dequant(W)^T in one pass: packed weights
+ * and scales
  * are streamed once, unpacked and decoded on chip and accumulated in FP32 against x; no
  * dequantised weight matrix is ever written ("LLM Quantization on RTX 4060", sections
  * "Fused Kernel: Moving Dequantization On-Chip" and "Kernel Implementation"; FP32
  * accumulation as that kernel's comment requires).  y is rounded to FP16 (nearest even).
- * Batches 1 ... 8 run on CUDA cores; batches 9 ... 128 on the 5th-generation tensor cores
- * (tcgen05) when K is a multiple of 64, else on CUDA cores.  Larger batches (prefill-sized,
- * up to W4_MAX_BATCH) run as tiles of 128 batch rows, each tile one pass over the weights.
+ * Batches 1 ... 8 run in the persistent small-batch kernel (weights decoded through a byte-pair
+ * table into warp-level mma.sync FP16 x FP16 -> FP32 products, block scales applied to the FP32
+ * partial sums); batches 9 ... 128 on the 5th-generation tensor cores (tcgen05) when K is a
+ * multiple of 64, else in 8-row launches of the small-batch kernel.  Larger batches
+ * (prefill-sized, up to W4_MAX_BATCH) run as tiles of 128 batch rows, each tile one pass over
+ * the weights.
  * Sizes: 1 <= M <= W4_MAX_BATCH, N >= 1, 32 <= K <= W4_MAX_K, K % blocksize == 0,
  * blocksize a power of two in [32, 256].  packed, scales, x 16-byte aligned; y 2-byte aligned.
  * Agreement with the float64 definition: relative L2 error <= 1e-3 and
- * max |error| <= 2e-2 * RMS(y) per output vector.  The tensor-core paths multiply in FP16, so
- * for them an NF4 absmax must stay below 65504 (the FP16 range; the FP32 absmax is rounded
- * to FP16) and so must every |x| and every decoded weight.
+ * max |error| <= 2e-2 * RMS(y) per output vector, under these conditions:
+ *   all paths: every |x| <= 65504 (FP16 inputs) and |y| within the FP16 range;
+ *   batches 1 ... 8: no condition on the scales (NF4 code values rounded to FP16, INT4 and FP4
+ *     values exact in FP16; the FP32 / FP16 block scale multiplies the FP32 partial sum);
+ *   batches 9 ... 128 (tcgen05, and the mma.sync fallback): each decoded weight is formed in
+ *     FP16 as fp16(value) * fp16(scale), so an NF4 absmax must lie in [6.1e-5, 65504] (the FP16
+ *     normal range; below it the rounded scale keeps fewer than 11 significant bits) and every
+ *     decoded weight must stay below 65504; INT4 and FP4 scales are FP16 already.
  */
 int w4_gemv_nf4(const uint8_t* packed, const float* absmax, const float* codebook,
                 const uint16_t* x, uint16_t* y, int M, int N, int K, int blocksize,
@@ -134,19 +161,22 @@ int w4_gemv_nf4(const uint8_t* packed, const float* absmax, const float* codeboo
 int w4_gemv_int4(const uint8_t* packed, const uint16_t* scale,
                  const uint16_t* x, uint16_t* y, int M, int N, int K, int group,
                  w4_stream_t stream);
+int w4_gemv_fp4(const uint8_t* packed, const uint16_t* scale,
+                const uint16_t* x, uint16_t* y, int M, int N, int K, int group,
+                w4_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
- * w4_gemv_plan -- which kernel w4_gemv_nf4 / w4_gemv_int4 would run for these sizes, and its
+ * w4_gemv_plan -- which kernel w4_gemv_nf4 / _int4 / _fp4 would run for these sizes, and its
  * launch geometry, on a GPU with sm_count SMs (152 on GB300).  The batch-driven choice of
  * path is the one "Do Quantization and Sparsity make LLM Inference Faster ?" describes for
  * bitsandbytes (section "NF4: fast at batch 1, slower at larger batches").  Host only: no
  * device call, nothing allocated; *plan is caller-owned and fully written on W4_OK.
- *   kernel      W4_KERNEL_CUDA_CORES or W4_KERNEL_TCGEN05
- *   launches    kernel launches the call makes (CUDA cores: one per <= batch_tile rows;
+ *   kernel      W4_KERNEL_SMALL_BATCH or W4_KERNEL_TCGEN05
+ *   launches    kernel launches the call makes (small-batch kernel: one per <= batch_tile rows;
  *               batches above 128: one set per 128-row batch tile)
- *   batch_tile  batch rows per launch (CUDA cores) or MMA N columns (tcgen05: 16/32/64/128)
+ *   batch_tile  batch rows per launch (small-batch kernel) or MMA N columns (tcgen05: 16/32/64/128)
  *   threads     threads per CTA; smem_bytes: dynamic shared memory per CTA
- *   stages      ring stages (CUDA cores: packed tiles; tcgen05: x / A stages)
+ *   stages      ring stages (small-batch kernel: packed tiles; tcgen05: x / A stages)
  *   grid        CTAs per launch (tcgen05), or 0 where the launch sizes it from occupancy
  *   cluster     CTAs per thread-block cluster splitting K (1: no split)
  * The figures are those of the widest launch.  The mma.sync tensor-core
@@ -155,7 +185,7 @@ int w4_gemv_int4(const uint8_t* packed, const uint16_t* scale,
  * no kernel takes), W4_ERR_SHAPE / W4_ERR_BLOCKSIZE as for the GEMV, W4_ERR_SHAPE for
  * sm_count < 1.
  */
-typedef enum { W4_KERNEL_CUDA_CORES = 1, W4_KERNEL_TCGEN05 = 2 } w4_kernel;
+typedef enum { W4_KERNEL_SMALL_BATCH = 1, W4_KERNEL_TCGEN05 = 2 } w4_kernel;
 typedef struct {
   int kernel, launches, batch_tile, threads, smem_bytes, stages, grid, cluster;
 } w4_gemv_plan_t;
@@ -171,8 +201,8 @@ int w4_gemv_plan(int format, int M, int N, int K, int blocksize, int sm_count, w
 typedef struct {
   int format;               /* w4_format                                               */
   const uint8_t* packed;    /* [N][K/2]                                                 */
-  const void* scales;       /* float absmax [N][K/bs] (NF4) or fp16 scale [N][K/gs] (INT4) */
-  const float* codebook;    /* [16] for NF4, ignored for INT4                           */
+  const void* scales;       /* float absmax [N][K/bs] (NF4) or fp16 scale [N][K/gs] (INT4, FP4) */
+  const float* codebook;    /* [16] for NF4, ignored otherwise                          */
   const uint16_t* x;        /* [M][K] fp16                                              */
   uint16_t* y;              /* [M][N] fp16                                              */
   int M, N, K, blocksize;
@@ -184,7 +214,9 @@ typedef struct {
 int w4_gemv_sequence(const w4_gemv_desc* descs, int count, w4_stream_t stream);
 
 /* Device workspace (bytes) that w4_step_create needs for `count` descriptors: one 32-bit counter
- * per level plus one. */
+ * per level plus one, then (128-byte aligned) the persistent launch's tables: one TMA tensor map
+ * per GEMV (128 bytes), the levels and the per-GEMV tiling (about 240 bytes per descriptor in
+ * all). */
 int64_t w4_step_workspace_bytes(int count);
 
 /* A decode step captured once into a CUDA graph.  When every descriptor has the same format,
@@ -192,8 +224,9 @@ int64_t w4_step_workspace_bytes(int count);
  * streams the weights of all levels ahead through its shared-memory ring and each level starts
  * reading x when the counters in `workspace` show the previous level complete.  Otherwise the
  * step is one launch per GEMV.  `workspace`: device memory of w4_step_workspace_bytes(count) bytes,
- * 16-byte aligned, owned by the caller, used only by this step; w4_step_create zeroes it (and
- * synchronises), every launch leaves it zero again.  Launches of one step must not overlap on
+ * 16-byte aligned, owned by the caller, used only by this step; w4_step_create zeroes the
+ * counters, writes the tables (and synchronises); every launch leaves the counters zero again and
+ * only reads the tables.  Launches of one step must not overlap on
  * the GPU (stream order guarantees that).  The descriptors' pointers are baked into the graph:
  * the buffers must outlive the step.  No device memory is allocated. */
 typedef struct w4_step w4_step;
@@ -210,16 +243,19 @@ int w4_step_destroy(w4_step* step);
  * allocator has reserved up front (a cudaMalloc there fails or fragments the pool), serving loops
  * that forbid allocation after warm-up (cudaMalloc can synchronise the device and stall every
  * stream), and plugin interfaces that hand the callee only its input and output buffers.
- * The level counters that w4_step_create keeps in a caller workspace live here in a fixed array
- * inside libw4 (W4_NOALLOC_MAX_LEVELS + 1 32-bit words, held on every GPU that loads the library
- * until the process exits).  Limits: at most W4_NOALLOC_MAX_LEVELS levels and W4_NOALLOC_MAX_GEMVS
+ * The level counters and tables that w4_step_create keeps in a caller workspace live here in
+ * fixed arrays inside libw4 (W4_NOALLOC_MAX_LEVELS + 1 32-bit words and about 61 KB of tables,
+ * held on every GPU that loads the library until the process exits).  Limits: at most W4_NOALLOC_MAX_LEVELS levels and W4_NOALLOC_MAX_GEMVS
  * descriptors, else W4_ERR_LIMIT.  Same conditions as the single-launch step (one format,
- * M <= 8, one code book), else W4_ERR_UNSUPPORTED.  Each call first clears the counters it uses
- * (an asynchronous memset on `stream`), then launches; it never calls cudaMalloc, cudaFree or
- * any allocating routine.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture.  Every call uses the same array, so calls that overlap on the GPU (other streams,
- * other host threads) race and give wrong results: serialise them. */
+ * M <= 8, one code book), else W4_ERR_UNSUPPORTED.  Each call first copies its tables in and
+ * clears the counters it uses (an asynchronous copy from pageable host memory and a memset on
+ * `stream`), then launches; it never calls cudaMalloc, cudaFree or any allocating routine.  The
+ * first call on a device looks up the arrays' device addresses (cudaGetSymbolAddress) with that
+ * device current and keeps them for the life of the process; make that first call before any
+ * stream capture, and do not call this entry point after cudaDeviceReset on that device (the
+ * kept addresses belong to the context the reset destroyed).  Every call uses the same arrays,
+ * so calls that overlap on the GPU (other streams, other host threads) race and give wrong
+ * results: serialise them. */
 #define W4_NOALLOC_MAX_LEVELS 256
 #define W4_NOALLOC_MAX_GEMVS 256
 int w4_gemv_levels_noalloc(const w4_gemv_desc* descs, int count, w4_stream_t stream);

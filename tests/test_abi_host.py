@@ -119,17 +119,17 @@ def _plan(fmt, m, n, k, bs, sms=SMS):
     return p
 
 
-@pytest.mark.parametrize("fmt,bs", [(w4.W4_FMT_NF4, 64), (w4.W4_FMT_INT4, 128)])
-def test_plan_batches_up_to_8_stay_on_cuda_cores(libw4, fmt, bs):
+@pytest.mark.parametrize("fmt,bs", [(w4.W4_FMT_NF4, 64), (w4.W4_FMT_INT4, 128), (w4.W4_FMT_FP4, 32)])
+def test_plan_batches_up_to_8_stay_on_the_small_batch_kernel(libw4, fmt, bs):
     for m in range(1, 9):
         for n, k in DECODE.values():
             p = _plan(fmt, m, n, k, bs)
-            assert p["kernel"] == w4.W4_KERNEL_CUDA_CORES and p["launches"] == 1 and p["batch_tile"] == m
+            assert p["kernel"] == w4.W4_KERNEL_SMALL_BATCH and p["launches"] == 1 and p["batch_tile"] == m
             assert p["cluster"] == 1 and p["smem_bytes"] <= 227 * 1024 and p["stages"] >= 2
 
 
 @pytest.mark.parametrize("fmt,bs", [(w4.W4_FMT_NF4, 64), (w4.W4_FMT_INT4, 128), (w4.W4_FMT_NF4, 32),
-                                    (w4.W4_FMT_INT4, 256)])
+                                    (w4.W4_FMT_INT4, 256), (w4.W4_FMT_FP4, 32)])
 def test_plan_tcgen05_resources(libw4, fmt, bs):
     for m in list(range(9, 129, 7)) + [16, 17, 32, 33, 64, 65, 128]:
         for n, k in list(DECODE.values()) + [(1, 256), (129, 64), (300, 320), (70, 8960)]:
@@ -178,16 +178,17 @@ def test_plan_split_choices_on_the_decode_shapes(libw4):
 def test_plan_shapes_the_tensor_cores_do_not_take(libw4):
     # K not a multiple of 64: CUDA-core launches of at most 8 batch rows
     p = _plan(w4.W4_FMT_NF4, 40, 100, 96, 32)
-    assert p["kernel"] == w4.W4_KERNEL_CUDA_CORES and p["launches"] == 5 and p["batch_tile"] == 8
+    assert p["kernel"] == w4.W4_KERNEL_SMALL_BATCH and p["launches"] == 5 and p["batch_tile"] == 8
     p = _plan(w4.W4_FMT_INT4, 20, 100, 160, 32)
-    assert p["kernel"] == w4.W4_KERNEL_CUDA_CORES and p["launches"] == 3
+    assert p["kernel"] == w4.W4_KERNEL_SMALL_BATCH and p["launches"] == 3
 
 
 def test_plan_validation(libw4):
     out = w4.GemvPlan()
     ref = ctypes.byref(out)
     assert libw4.w4_gemv_plan(0, 1, 16, 64, 64, SMS, None) == w4.W4_ERR_NULL
-    assert libw4.w4_gemv_plan(2, 1, 16, 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED
+    assert libw4.w4_gemv_plan(3, 1, 16, 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED
+    assert libw4.w4_gemv_plan(w4.W4_FMT_FP4, 1, 16, 64, 32, SMS, ref) == w4.W4_OK
     assert libw4.w4_gemv_plan(0, 0, 16, 64, 64, SMS, ref) == w4.W4_ERR_SHAPE
     assert libw4.w4_gemv_plan(0, 4097, 16, 64, 64, SMS, ref) == w4.W4_ERR_UNSUPPORTED
     assert libw4.w4_gemv_plan(0, 1, 0, 64, 64, SMS, ref) == w4.W4_ERR_SHAPE

@@ -42,7 +42,8 @@ def gpu_quantize(fmt, w, bs, dev):
         w4.check(w4.w4_quantize_nf4(W, packed, sc, _code(dev), n, k, bs))
     else:
         sc = torch.empty((n, k // bs), dtype=torch.float16, device=dev)
-        w4.check(w4.w4_quantize_int4(W, packed, sc, n, k, bs))
+        quant = w4.w4_quantize_int4 if fmt == "int4" else w4.w4_quantize_fp4
+        w4.check(quant(W, packed, sc, n, k, bs))
     return packed, sc
 
 
@@ -51,24 +52,46 @@ def gpu_gemv(fmt, packed, sc, x, n, k, bs, dev, y=None):
     X = _t(x, dev)
     if y is None:
         y = torch.full((m, n), float("nan"), dtype=torch.float16, device=dev)
-    if fmt == "nf4":
-        w4.check(w4.w4_gemv_nf4(packed, sc, _code(dev), X, y, m, n, k, bs))
-    else:
-        w4.check(w4.w4_gemv_int4(packed, sc, X, y, m, n, k, bs))
+    launch_gemv(fmt, packed, sc, X, y, m, n, k, bs, dev)
     torch.cuda.synchronize()
     return y
+
+
+def launch_gemv(fmt, packed, sc, X, y, m, n, k, bs, dev):
+    if fmt == "nf4":
+        w4.check(w4.w4_gemv_nf4(packed, sc, _code(dev), X, y, m, n, k, bs))
+    elif fmt == "int4":
+        w4.check(w4.w4_gemv_int4(packed, sc, X, y, m, n, k, bs))
+    else:
+        w4.check(w4.w4_gemv_fp4(packed, sc, X, y, m, n, k, bs))
+
+
+# default block / group size of each format
+BS = {"nf4": 64, "int4": 128, "fp4": 32}
 
 
 def oracle_quantize(fmt, w, bs):
     if fmt == "nf4":
         return oracle.quantize_nf4(w, oracle.nf4_codebook(), bs)
-    return oracle.quantize_int4(w, bs)
+    if fmt == "int4":
+        return oracle.quantize_int4(w, bs)
+    return oracle.quantize_fp4(w, bs)
+
+
+def oracle_dequantize(fmt, packed, sc, bs):
+    if fmt == "nf4":
+        return oracle.dequantize_nf4(packed, sc, oracle.nf4_codebook(), bs)
+    if fmt == "int4":
+        return oracle.dequantize_int4(packed, sc, bs)
+    return oracle.dequantize_fp4(packed, sc, bs)
 
 
 def oracle_gemv(fmt, packed, sc, x, bs, rows=None):
     if fmt == "nf4":
         return oracle.gemv_nf4(packed, sc, oracle.nf4_codebook(), x, bs, rows=rows)
-    return oracle.gemv_int4(packed, sc, x, bs, rows=rows)
+    if fmt == "int4":
+        return oracle.gemv_int4(packed, sc, x, bs, rows=rows)
+    return oracle.gemv_fp4(packed, sc, x, bs, rows=rows)
 
 
 def assert_gemv_close(y, y_ref):
@@ -88,6 +111,8 @@ QUANT_CASES = [
     ("nf4", 5, 256, 32), ("nf4", 7, 512, 128), ("nf4", 2, 512, 256),
     ("int4", 1, 128, 128), ("int4", 3, 256, 128), ("int4", 257, 1536, 128), ("int4", 16, 8960, 128),
     ("int4", 5, 256, 32), ("int4", 7, 512, 64), ("int4", 2, 512, 256),
+    ("fp4", 1, 32, 32), ("fp4", 3, 128, 32), ("fp4", 257, 1536, 32), ("fp4", 16, 8960, 32),
+    ("fp4", 5, 256, 64), ("fp4", 7, 512, 128), ("fp4", 2, 512, 256),
 ]
 
 
@@ -102,7 +127,7 @@ def test_quantize_bit_exact(dev, fmt, n, k, bs):
     assert got.dtype == s_ref.dtype and np.array_equal(got.view(np.uint8), s_ref.view(np.uint8))
 
 
-@pytest.mark.parametrize("fmt,bs", [("nf4", 64), ("int4", 128)])
+@pytest.mark.parametrize("fmt,bs", [("nf4", 64), ("int4", 128), ("fp4", 32)])
 def test_quantize_ties_and_grid_points(dev, fmt, bs):
     """Values exactly on code points and exactly at rounding boundaries."""
     code = oracle.nf4_codebook()
@@ -114,12 +139,22 @@ def test_quantize_ties_and_grid_points(dev, fmt, bs):
         mids = ((code[:-1].astype(np.float64) + code[1:]) / 2 * float(a)).astype(np.float32)
         r = np.zeros(64, np.float32); r[:15] = mids; r[15] = a
         rows.append(r)
-    else:
+    elif fmt == "int4":
         s = 2.0 ** -6
         t = np.array([2.5, 3.5, -2.5, -3.5, 0.5, -0.5, 1.5, 6.5, -6.5], np.float64)
         r = np.zeros(128, np.float32); r[: len(t)] = (t * s).astype(np.float32); r[127] = 7 * s
         rows.append(r)
         rows.append(((np.arange(128) % 15 - 7) * s).astype(np.float32))
+    else:
+        s = 2.0 ** -4
+        grid = oracle.fp4_grid()
+        mids = (grid[:-1] + grid[1:]) / 2
+        r = np.zeros(32, np.float32)
+        r[:7] = mids * s; r[7:14] = -mids * s; r[31] = 6 * s
+        r[14:21] = np.nextafter((mids * s).astype(np.float32), np.float32(1))
+        r[21:28] = np.nextafter((mids * s).astype(np.float32), np.float32(0))
+        rows.append(r)
+        rows.append(np.concatenate([grid, -grid[1:], grid, -grid[1:], [6.0, -6.0]]).astype(np.float32) * np.float32(s))
     w = np.stack(rows)
     packed, sc = gpu_quantize(fmt, w, bs, dev)
     p_ref, s_ref = oracle_quantize(fmt, w, bs)
@@ -135,10 +170,11 @@ def test_dequantize_bit_exact(dev, fmt, n, k, bs):
     out = torch.empty((n, k), dtype=torch.float32, device=dev)
     if fmt == "nf4":
         w4.check(w4.w4_dequantize_nf4(packed, sc, _code(dev), out, n, k, bs))
-        ref = oracle.dequantize_nf4(p_ref, s_ref, oracle.nf4_codebook(), bs)
-    else:
+    elif fmt == "int4":
         w4.check(w4.w4_dequantize_int4(packed, sc, out, n, k, bs))
-        ref = oracle.dequantize_int4(p_ref, s_ref, bs)
+    else:
+        w4.check(w4.w4_dequantize_fp4(packed, sc, out, n, k, bs))
+    ref = oracle_dequantize(fmt, p_ref, s_ref, bs)
     torch.cuda.synchronize()
     assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
@@ -156,6 +192,10 @@ GEMV_CASES = [
     # an odd number of chunks per row and of batch rows x chunks (shared-memory layouts whose
     # parts are not multiples of 16 bytes)
     ("nf4", 1, 45, 96, 32), ("int4", 1, 45, 96, 32), ("int4", 3, 40, 160, 32), ("nf4", 3, 40, 160, 32),
+    ("fp4", 1, 1, 64, 32), ("fp4", 1, 257, 1536, 32), ("fp4", 1, 1536, 1536, 32), ("fp4", 1, 100, 8960, 32),
+    ("fp4", 2, 333, 1536, 32), ("fp4", 3, 64, 8960, 32), ("fp4", 4, 1000, 1536, 32), ("fp4", 8, 777, 1536, 32),
+    ("fp4", 8, 61, 8960, 32), ("fp4", 1, 70, 512, 64), ("fp4", 2, 70, 1024, 128), ("fp4", 1, 45, 96, 32),
+    ("fp4", 3, 40, 160, 32), ("fp4", 5, 129, 1536, 256),
 ]
 
 
@@ -181,6 +221,8 @@ TC_CASES = [
     ("nf4", 100, 300, 1536, 128), ("nf4", 128, 1536, 1536, 64), ("nf4", 128, 70, 8960, 256),
     ("int4", 32, 8960, 1536, 128), ("int4", 32, 1536, 8960, 128), ("int4", 47, 257, 1536, 64),
     ("int4", 128, 1536, 1536, 128), ("int4", 96, 130, 8960, 32),
+    ("fp4", 16, 256, 1536, 32), ("fp4", 9, 8960, 1536, 32), ("fp4", 32, 1536, 8960, 32), ("fp4", 64, 129, 512, 64),
+    ("fp4", 128, 1536, 1536, 32), ("fp4", 130, 257, 1024, 32), ("fp4", 20, 100, 160, 32), ("fp4", 40, 100, 96, 32),
 ]
 
 
@@ -198,10 +240,10 @@ def test_tensor_core_batches(dev, fmt, m, n, k, bs):
     assert np.array_equal(y.view(np.uint16), y2.view(np.uint16))
 
 
-@pytest.mark.parametrize("fmt", ["nf4", "int4"])
+@pytest.mark.parametrize("fmt", ["nf4", "int4", "fp4"])
 @pytest.mark.parametrize("m", [12, 20, 32, 64, 128])
 def test_gemv_parity_larger_batches(dev, fmt, m):
-    bs = 64 if fmt == "nf4" else 128
+    bs = BS[fmt]
     n, k = 300, 1536
     w = synth.weights(5000 + m, n, k)
     x = synth.activations(5100 + m, m, k)
@@ -210,23 +252,24 @@ def test_gemv_parity_larger_batches(dev, fmt, m):
     assert_gemv_close(y.cpu().numpy(), oracle_gemv(fmt, p_ref, s_ref, x, bs))
 
 
-@pytest.mark.parametrize("fmt", ["nf4", "int4"])
+@pytest.mark.parametrize("fmt", ["nf4", "int4", "fp4"])
 def test_gemv_one_hot_zero_linearity_idempotence(dev, fmt):
-    bs = 64 if fmt == "nf4" else 128
+    bs = BS[fmt]
     n, k = 96, 1536
     w = synth.weights(6000, n, k)
     p_ref, s_ref = oracle_quantize(fmt, w, bs)
     packed, sc = _t(p_ref, dev), _t(s_ref, dev)
-    wh = oracle.dequantize_nf4(p_ref, s_ref, oracle.nf4_codebook(), bs) if fmt == "nf4" else \
-        oracle.dequantize_int4(p_ref, s_ref, bs)
+    wh = oracle_dequantize(fmt, p_ref, s_ref, bs)
     # one-hot x picks column k of w_hat: pins nibble order, block index and orientation
     for kk in (0, 1, 63, 64, 1535):
         x = np.zeros((1, k), np.float16)
         x[0, kk] = 1.0
         y = gpu_gemv(fmt, packed, sc, x, n, k, bs, dev).cpu().numpy()[0]
         exp = wh[:, kk].astype(np.float16)
-        if fmt == "int4":
-            assert np.array_equal(y.view(np.uint16), exp.view(np.uint16))        # exact path
+        if fmt != "nf4":
+            # exact path: equal values (bit for bit except that -0 and +0 are both accepted: an
+            # FP4 code 8 decodes to -0, and a sum starting from +0 gives +0)
+            assert np.array_equal(y, exp)
         else:
             assert np.allclose(y.astype(np.float64), wh[:, kk], rtol=2 ** -10, atol=0)
     # zero input gives exactly zero
@@ -241,17 +284,14 @@ def test_gemv_one_hot_zero_linearity_idempotence(dev, fmt):
     X = _t(x, dev)
     ya = torch.full((2, n), 7.0, dtype=torch.float16, device=dev)
     for _ in range(2):
-        if fmt == "nf4":
-            w4.check(w4.w4_gemv_nf4(packed, sc, _code(dev), X, ya, 2, n, k, bs))
-        else:
-            w4.check(w4.w4_gemv_int4(packed, sc, X, ya, 2, n, k, bs))
+        launch_gemv(fmt, packed, sc, X, ya, 2, n, k, bs, dev)
         torch.cuda.synchronize()
         assert np.array_equal(ya.cpu().numpy().view(np.uint16), y1.view(np.uint16))
 
 
-@pytest.mark.parametrize("fmt", ["nf4", "int4"])
+@pytest.mark.parametrize("fmt", ["nf4", "int4", "fp4"])
 def test_gemv_writes_nothing_outside_y(dev, fmt):
-    bs = 64 if fmt == "nf4" else 128
+    bs = BS[fmt]
     n, k, m = 131, 1536, 3
     w = synth.weights(7000, n, k)
     x = synth.activations(7001, m, k)
@@ -265,11 +305,11 @@ def test_gemv_writes_nothing_outside_y(dev, fmt):
     assert_gemv_close(y.cpu().numpy(), oracle_gemv(fmt, p_ref, s_ref, x, bs))
 
 
-@pytest.mark.parametrize("fmt", ["nf4", "int4"])
+@pytest.mark.parametrize("fmt", ["nf4", "int4", "fp4"])
 def test_decode_shapes_full_size_sampled(dev, fmt):
     """Every decode-step shape at full size, quantised on the GPU; sampled output rows checked
     one by one against the oracle (which quantises those rows itself)."""
-    bs = 64 if fmt == "nf4" else 128
+    bs = BS[fmt]
     rng = np.random.default_rng(8)
     for name, n, k, _ in synth.DECODE_SHAPES:
         w = synth.weights(synth.weight_seed(0 if name != "lm_head" else 28, name), n, k)

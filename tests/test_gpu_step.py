@@ -28,9 +28,12 @@ def _check_step(step, rows_per_gemv=8, seed=0):
         if step.fmt == "nf4":
             p, s = oracle.quantize_nf4(w, code, step.bs)
             y_ref = oracle.gemv_nf4(p, s, code, x, step.bs)
-        else:
+        elif step.fmt == "int4":
             p, s = oracle.quantize_int4(w, step.bs)
             y_ref = oracle.gemv_int4(p, s, x, step.bs)
+        else:
+            p, s = oracle.quantize_fp4(w, step.bs)
+            y_ref = oracle.gemv_fp4(p, s, x, step.bs)
         y = step.y_of(i).cpu().numpy()[:, rows].astype(np.float64)
         rms = np.sqrt(np.mean(y_ref ** 2, axis=1, keepdims=True))
         assert np.all(np.abs(y - y_ref) <= 2e-2 * rms), (layer, proj)
@@ -38,7 +41,8 @@ def _check_step(step, rows_per_gemv=8, seed=0):
         assert np.all(rel <= 1e-3), (layer, proj, rel)
 
 
-@pytest.mark.parametrize("fmt,levels", [("nf4", "grouped"), ("nf4", "strict"), ("int4", "grouped")])
+@pytest.mark.parametrize("fmt,levels", [("nf4", "grouped"), ("nf4", "strict"), ("int4", "grouped"),
+                                        ("fp4", "grouped")])
 def test_full_step_graph(dev, fmt, levels):
     """The whole 197-GEMV step (113 levels grouped, 197 strict) in one persistent launch."""
     from weight_only_bit_gb300.step import DecodeStep
@@ -70,7 +74,8 @@ def test_full_step_graph(dev, fmt, levels):
     step.close()
 
 
-@pytest.mark.parametrize("fmt,batch", [("int4", 1), ("nf4", 3), ("nf4", 8), ("int4", 8), ("nf4", 32)])
+@pytest.mark.parametrize("fmt,batch", [("int4", 1), ("nf4", 3), ("nf4", 8), ("int4", 8), ("nf4", 32), ("fp4", 2),
+                                       ("fp4", 8), ("fp4", 32)])
 def test_reduced_steps(dev, fmt, batch):
     from weight_only_bit_gb300.step import DecodeStep
     step = DecodeStep(fmt, batch=batch, device=str(dev), layers=2, lm_head=False,

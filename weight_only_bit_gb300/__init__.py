@@ -11,7 +11,7 @@ import ctypes
 
 from ._lib import (GemvDesc, GemvPlan, W4Error, lib, SYMBOLS, W4_OK, W4_ERR_NULL, W4_ERR_SHAPE, W4_ERR_ALIGN,
                    W4_ERR_BLOCKSIZE, W4_ERR_CUDA, W4_ERR_TIMEOUT, W4_ERR_UNSUPPORTED, W4_FMT_NF4,
-                   W4_FMT_INT4, W4_MAX_BATCH, W4_MAX_K, W4_KERNEL_CUDA_CORES, W4_KERNEL_TCGEN05)
+                   W4_FMT_INT4, W4_FMT_FP4, W4_MAX_BATCH, W4_MAX_K, W4_KERNEL_SMALL_BATCH, W4_KERNEL_TCGEN05)
 
 __all__ = [
     "w4_nf4_codebook", "w4_quantize_nf4", "w4_quantize_int4", "w4_dequantize_nf4", "w4_dequantize_int4",
@@ -19,8 +19,10 @@ __all__ = [
     "w4_step_launch",
     "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check", "w4_launch_count",
     "w4_inject_timeout_once", "w4_gemv_levels_noalloc", "w4_gemv_plan",
-    "check", "W4Error", "GemvDesc", "GemvPlan", "W4_FMT_NF4", "W4_FMT_INT4", "W4_MAX_BATCH", "W4_MAX_K",
-    "W4_KERNEL_CUDA_CORES", "W4_KERNEL_TCGEN05",
+    "w4_quantize_fp4", "w4_dequantize_fp4", "w4_gemv_fp4",
+    "check", "W4Error", "GemvDesc", "GemvPlan", "W4_FMT_NF4", "W4_FMT_INT4", "W4_FMT_FP4", "W4_MAX_BATCH",
+    "W4_MAX_K",
+    "W4_KERNEL_SMALL_BATCH", "W4_KERNEL_TCGEN05",
 ]
 
 
@@ -63,6 +65,10 @@ def w4_quantize_int4(W, packed, scale, N, K, group=128, stream=None):
     return lib().w4_quantize_int4(_ptr(W), _ptr(packed), _ptr(scale), N, K, group, _stream(stream))
 
 
+def w4_quantize_fp4(W, packed, scale, N, K, group=32, stream=None):
+    return lib().w4_quantize_fp4(_ptr(W), _ptr(packed), _ptr(scale), N, K, group, _stream(stream))
+
+
 def w4_dequantize_nf4(packed, absmax, codebook, W_out, N, K, blocksize=64, stream=None):
     return lib().w4_dequantize_nf4(_ptr(packed), _ptr(absmax), _ptr(codebook), _ptr(W_out), N, K, blocksize,
                                    _stream(stream))
@@ -72,6 +78,10 @@ def w4_dequantize_int4(packed, scale, W_out, N, K, group=128, stream=None):
     return lib().w4_dequantize_int4(_ptr(packed), _ptr(scale), _ptr(W_out), N, K, group, _stream(stream))
 
 
+def w4_dequantize_fp4(packed, scale, W_out, N, K, group=32, stream=None):
+    return lib().w4_dequantize_fp4(_ptr(packed), _ptr(scale), _ptr(W_out), N, K, group, _stream(stream))
+
+
 def w4_gemv_nf4(packed, absmax, codebook, x, y, M, N, K, blocksize=64, stream=None):
     return lib().w4_gemv_nf4(_ptr(packed), _ptr(absmax), _ptr(codebook), _ptr(x), _ptr(y), M, N, K, blocksize,
                              _stream(stream))
@@ -79,6 +89,10 @@ def w4_gemv_nf4(packed, absmax, codebook, x, y, M, N, K, blocksize=64, stream=No
 
 def w4_gemv_int4(packed, scale, x, y, M, N, K, group=128, stream=None):
     return lib().w4_gemv_int4(_ptr(packed), _ptr(scale), _ptr(x), _ptr(y), M, N, K, group, _stream(stream))
+
+
+def w4_gemv_fp4(packed, scale, x, y, M, N, K, group=32, stream=None):
+    return lib().w4_gemv_fp4(_ptr(packed), _ptr(scale), _ptr(x), _ptr(y), M, N, K, group, _stream(stream))
 
 
 def _descs(descs):

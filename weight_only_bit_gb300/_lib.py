@@ -24,7 +24,8 @@ W4_NOALLOC_MAX_LEVELS = 256
 W4_NOALLOC_MAX_GEMVS = 256
 W4_FMT_NF4 = 0
 W4_FMT_INT4 = 1
-W4_KERNEL_CUDA_CORES = 1
+W4_FMT_FP4 = 2
+W4_KERNEL_SMALL_BATCH = 1
 W4_KERNEL_TCGEN05 = 2
 W4_MAX_BATCH = 4096
 W4_MAX_K = 10240
@@ -35,6 +36,7 @@ SYMBOLS = (
     "w4_dequantize_int4", "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_workspace_bytes", "w4_step_create",
     "w4_step_launch", "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check",
     "w4_launch_count", "w4_inject_timeout_once", "w4_gemv_levels_noalloc", "w4_gemv_plan",
+    "w4_quantize_fp4", "w4_dequantize_fp4", "w4_gemv_fp4",
 )
 
 
@@ -89,6 +91,9 @@ def _declare(L):
         "w4_dequantize_int4": (I, [P, P, P, I, I, I, P]),
         "w4_gemv_nf4": (I, [P, P, P, P, P, I, I, I, I, P]),
         "w4_gemv_int4": (I, [P, P, P, P, I, I, I, I, P]),
+        "w4_quantize_fp4": (I, [P, P, P, I, I, I, P]),
+        "w4_dequantize_fp4": (I, [P, P, P, I, I, I, P]),
+        "w4_gemv_fp4": (I, [P, P, P, P, I, I, I, I, P]),
         "w4_gemv_sequence": (I, [ctypes.POINTER(GemvDesc), I, P]),
         "w4_step_workspace_bytes": (ctypes.c_int64, [I]),
         "w4_step_create": (I, [ctypes.POINTER(GemvDesc), I, P, ctypes.POINTER(P)]),

@@ -47,7 +47,7 @@ int check_shape(int N, int K, int bs) {
 
 int check_gemv(int format, const uint8_t* packed, const void* scales, const float* codebook, const uint16_t* x,
                const uint16_t* y, int M, int N, int K, int bs) {
-  if (format != W4_FMT_NF4 && format != W4_FMT_INT4) return W4_ERR_UNSUPPORTED;
+  if (format != W4_FMT_NF4 && format != W4_FMT_INT4 && format != W4_FMT_FP4) return W4_ERR_UNSUPPORTED;
   if (!packed || !scales || !x || !y || (format == W4_FMT_NF4 && !codebook)) return W4_ERR_NULL;
   int s = check_shape(N, K, bs);
   if (s != W4_OK) return s;
@@ -174,6 +174,16 @@ int w4_quantize_int4(const float* W, uint8_t* packed, uint16_t* scale, int N, in
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int w4_quantize_fp4(const float* W, uint8_t* packed, uint16_t* scale, int N, int K, int group,
+                    w4_stream_t stream) {
+  if (!W || !packed || !scale) return W4_ERR_NULL;
+  int s = check_shape(N, K, group);
+  if (s != W4_OK) return s;
+  if (!aligned(W, 16) || !aligned(packed, 16) || !aligned(scale, 16)) return W4_ERR_ALIGN;
+  return cuda_status(w4::launch_quantize_fp4(W, packed, reinterpret_cast<__half*>(scale), N, K, group,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int w4_dequantize_nf4(const uint8_t* packed, const float* absmax, const float* codebook, float* W_out, int N,
                       int K, int blocksize, w4_stream_t stream) {
   if (!packed || !absmax || !codebook || !W_out) return W4_ERR_NULL;
@@ -194,6 +204,16 @@ int w4_dequantize_int4(const uint8_t* packed, const uint16_t* scale, float* W_ou
                                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int w4_dequantize_fp4(const uint8_t* packed, const uint16_t* scale, float* W_out, int N, int K, int group,
+                      w4_stream_t stream) {
+  if (!packed || !scale || !W_out) return W4_ERR_NULL;
+  int s = check_shape(N, K, group);
+  if (s != W4_OK) return s;
+  if (!aligned(W_out, 8) || !aligned(packed, 16) || !aligned(scale, 16)) return W4_ERR_ALIGN;
+  return cuda_status(w4::launch_dequantize_fp4(packed, reinterpret_cast<const __half*>(scale), W_out, N, K, group,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int w4_gemv_nf4(const uint8_t* packed, const float* absmax, const float* codebook, const uint16_t* x, uint16_t* y,
                 int M, int N, int K, int blocksize, w4_stream_t stream) {
   int s = check_gemv(W4_FMT_NF4, packed, absmax, codebook, x, y, M, N, K, blocksize);
@@ -207,6 +227,14 @@ int w4_gemv_int4(const uint8_t* packed, const uint16_t* scale, const uint16_t* x
   int s = check_gemv(W4_FMT_INT4, packed, scale, nullptr, x, y, M, N, K, group);
   if (s != W4_OK) return s;
   return enqueue_gemv(W4_FMT_INT4, packed, scale, nullptr, x, y, M, N, K, group,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+int w4_gemv_fp4(const uint8_t* packed, const uint16_t* scale, const uint16_t* x, uint16_t* y, int M, int N, int K,
+                int group, w4_stream_t stream) {
+  int s = check_gemv(W4_FMT_FP4, packed, scale, nullptr, x, y, M, N, K, group);
+  if (s != W4_OK) return s;
+  return enqueue_gemv(W4_FMT_FP4, packed, scale, nullptr, x, y, M, N, K, group,
                       reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -234,13 +262,13 @@ static int plan_tile(int format, int M, int N, int K, int blocksize, int sm_coun
   }
   w4::SimtPlan sp;
   if (!w4::plan_simt(format, M, K, blocksize, &sp)) return W4_ERR_UNSUPPORTED;
-  *plan = w4_gemv_plan_t{W4_KERNEL_CUDA_CORES, sp.launches, sp.mb, sp.threads, sp.smem, sp.stages, 0, 1};
+  *plan = w4_gemv_plan_t{W4_KERNEL_SMALL_BATCH, sp.launches, sp.mb, sp.threads, sp.smem, sp.stages, 0, 1};
   return W4_OK;
 }
 
 int w4_gemv_plan(int format, int M, int N, int K, int blocksize, int sm_count, w4_gemv_plan_t* plan) {
   if (!plan) return W4_ERR_NULL;
-  if (format != W4_FMT_NF4 && format != W4_FMT_INT4) return W4_ERR_UNSUPPORTED;
+  if (format != W4_FMT_NF4 && format != W4_FMT_INT4 && format != W4_FMT_FP4) return W4_ERR_UNSUPPORTED;
   int s = check_shape(N, K, blocksize);
   if (s != W4_OK) return s;
   if (M < 1 || sm_count < 1) return W4_ERR_SHAPE;

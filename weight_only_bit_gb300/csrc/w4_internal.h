@@ -17,6 +17,10 @@ cudaError_t launch_quantize_nf4(const float* W, uint8_t* packed, float* absmax, 
                                 int N, int K, int bs, cudaStream_t stream);
 cudaError_t launch_quantize_int4(const float* W, uint8_t* packed, __half* scale, int N, int K, int gs,
                                  cudaStream_t stream);
+cudaError_t launch_quantize_fp4(const float* W, uint8_t* packed, __half* scale, int N, int K, int gs,
+                                cudaStream_t stream);
+cudaError_t launch_dequantize_fp4(const uint8_t* packed, const __half* scale, float* out, int N, int K, int gs,
+                                  cudaStream_t stream);
 cudaError_t launch_dequantize_nf4(const uint8_t* packed, const float* absmax, const float* codebook,
                                   float* out, int N, int K, int bs, cudaStream_t stream);
 cudaError_t launch_dequantize_int4(const uint8_t* packed, const __half* scale, float* out, int N, int K,

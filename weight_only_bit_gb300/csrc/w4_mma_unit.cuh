@@ -52,28 +52,6 @@ __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lane, uint32_t w, int 
   return lds_table(lut_lane + (byte << 7));
 }
 
-// Byte-pair table for the format: entry b = half2(v(b >> 4), v(b & 15)), one copy per lane (entry b
-// of lane l at word 32 b + l, so any pattern of bytes across a warp is conflict-free).
-//   NF4: v(q) = fp16(code[q]);  INT4: v(q) = q - 8;  FP4 (E2M1, sign in bit 3): v(q) = +-{0, 0.5, 1,
-//   1.5, 2, 3, 4, 6}[q & 7] ("LLM Compressor 0.14", section "Details worth knowing": the E2M1 grid).
-__device__ __forceinline__ float nibble_value(int fmt, const float* __restrict__ codebook, int q) {
-  if (fmt == 0) return __ldg(codebook + q);
-  if (fmt == 1) return (float)(q - 8);
-  const int mag = q & 7;
-  const float v = mag < 4 ? 0.5f * (float)mag : (float)(1 << (mag - 2)) * (mag & 1 ? 1.5f : 1.0f);
-  return (q & 8) ? -v : v;
-}
-
-__device__ __forceinline__ void build_lut(uint32_t* lut, int fmt, const float* __restrict__ codebook, int t,
-                                          int nthreads) {
-  for (int i = t; i < 256 * 32; i += nthreads) {
-    const int b = i >> 5;
-    const __half lo = __float2half_rn(nibble_value(fmt, codebook, b >> 4));
-    const __half hi = __float2half_rn(nibble_value(fmt, codebook, b & 15));
-    lut[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-  }
-}
-
 // Sum of one output's partials rr[0 .. C) in order (16-byte loads; rr 16-byte aligned).
 __device__ __forceinline__ float sum_spans(const float* rr, int C) {
   float s = 0.0f;

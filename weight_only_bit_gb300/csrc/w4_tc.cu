@@ -12,8 +12,9 @@
 // y^T[N][M] = W_hat[N][K] . x^T[K][M] with mma.sync.m16n8k16 (FP16 x FP16 -> FP32):
 //   * A = weights.  Warp w of a CTA owns 16 rows.  A packed byte holds the element pair (2j, 2j+1)
 //     of one row, which is exactly one A-fragment register (two consecutive k of one row), so the
-//     byte-pair table of w4_decode.cuh (NF4 code values, or q - 8 for INT4) yields fragments
-//     directly; the block scale (FP32 absmax rounded to FP16, or the FP16 INT4 scale) multiplies
+//     byte-pair table of w4_decode.cuh (NF4 code values, q - 8 for INT4, E2M1 values for FP4) yields
+//     fragments
+//     directly; the block scale (FP32 absmax rounded to FP16, or the FP16 INT4 / FP4 scale) multiplies
 //     each fragment (one HMUL2 per two weights).
 //   * K is reordered identically for A and B: in each 64-k chunk, thread t (= lane % 4) owns the
 //     8 consecutive packed bytes 8t ... 8t+7 of its two rows (one 8-byte load each); in k-step s
@@ -114,19 +115,8 @@ __global__ void __launch_bounds__(kTcWarps * 32, NT >= 16 ? 1 : 2) w4_tc_kernel(
   const bool okA = rA < p.N, okB = rB < p.N;
   const int M = p.M;
 
-  // decode table: NF4 code values, or q - 8 for INT4 (both exact in FP16 for INT4)
-  for (int i = threadIdx.x; i < 256 * 32; i += blockDim.x) {
-    const int b = i >> 5;
-    __half lo, hi;
-    if (FMT == 0) {
-      lo = __float2half_rn(__ldg(p.codebook + (b >> 4)));
-      hi = __float2half_rn(__ldg(p.codebook + (b & 15)));
-    } else {
-      lo = __int2half_rn((b >> 4) - 8);
-      hi = __int2half_rn((b & 15) - 8);
-    }
-    lut[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-  }
+  // decode table: NF4 code values, q - 8 for INT4, E2M1 values for FP4
+  build_lut(lut, FMT, p.codebook, (int)threadIdx.x, (int)blockDim.x);
   const uint32_t lut_lane = smem_u32(lut) + (uint32_t)lane * 4u;
   pdl_launch_dependents();
   pdl_wait();
@@ -323,9 +313,14 @@ cudaError_t launch_gemv_tc(int format, const uint8_t* packed, const void* scales
     if (NT <= 8) return launch_tc_nt<0, 8>(p, pdl, stream);
     return launch_tc_nt<0, 16>(p, pdl, stream);
   }
-  if (NT <= 4) return launch_tc_nt<1, 4>(p, pdl, stream);
-  if (NT <= 8) return launch_tc_nt<1, 8>(p, pdl, stream);
-  return launch_tc_nt<1, 16>(p, pdl, stream);
+  if (format == 1) {
+    if (NT <= 4) return launch_tc_nt<1, 4>(p, pdl, stream);
+    if (NT <= 8) return launch_tc_nt<1, 8>(p, pdl, stream);
+    return launch_tc_nt<1, 16>(p, pdl, stream);
+  }
+  if (NT <= 4) return launch_tc_nt<2, 4>(p, pdl, stream);
+  if (NT <= 8) return launch_tc_nt<2, 8>(p, pdl, stream);
+  return launch_tc_nt<2, 16>(p, pdl, stream);
 }
 
 }  // namespace w4

@@ -11,7 +11,8 @@
 //     into a ring of shared-memory slots, 128-byte swizzled so that the decoders' reads are free
 //     of bank conflicts;
 //   * A = 128 weight rows x 64 k per stage, decoded by 512 threads (byte-pair table of
-//     w4_decode.cuh: NF4 code values, or q - 8 for INT4; times the block scale in FP16) and
+//     w4_decode.cuh: NF4 code values, q - 8 for INT4, E2M1 values for FP4; times the block scale
+//     in FP16) and
 //     stored straight into tensor memory (tcgen05.st): lane = weight row, 32 columns per stage,
 //     two FP16 k values per column.  The MMA reads A from tensor memory, so decoded weights never
 //     pass through shared memory (whose bandwidth the byte-pair table already uses);
@@ -259,18 +260,7 @@ __global__ void __launch_bounds__(kT5Threads, 1) w4_tc5_kernel(const __grid_cons
   constexpr int kEs = FMT == 0 ? 4 : 2;   // bytes per scale
 
   // ---- set-up: table, barriers, tensor memory
-  for (int i = tid; i < 256 * 32; i += kT5Threads) {
-    const int b = i >> 5;
-    __half lo, hi;
-    if (FMT == 0) {
-      lo = __float2half_rn(__ldg(p.codebook + (b >> 4)));
-      hi = __float2half_rn(__ldg(p.codebook + (b & 15)));
-    } else {
-      lo = __int2half_rn((b >> 4) - 8);
-      hi = __int2half_rn((b & 15) - 8);
-    }
-    lut[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-  }
+  build_lut(lut, FMT, p.codebook, tid, kT5Threads);
   if (tid == 0) {
     for (int i = 0; i < NP; ++i) {
       mbar_init(&pfull[i], 2);          // the TMA producer (with the bytes) and the scale warp
@@ -673,6 +663,10 @@ cudaError_t launch_gemv_tc5(int format, const uint8_t* packed, const void* scale
     case 1032: return launch_tc5_nb<1, 32>(p, pl, pdl, stream);
     case 1064: return launch_tc5_nb<1, 64>(p, pl, pdl, stream);
     case 1128: return launch_tc5_nb<1, 128>(p, pl, pdl, stream);
+    case 2016: return launch_tc5_nb<2, 16>(p, pl, pdl, stream);
+    case 2032: return launch_tc5_nb<2, 32>(p, pl, pdl, stream);
+    case 2064: return launch_tc5_nb<2, 64>(p, pl, pdl, stream);
+    case 2128: return launch_tc5_nb<2, 128>(p, pl, pdl, stream);
     default: return cudaErrorNotSupported;
   }
 }

@@ -31,8 +31,8 @@ class DecodeStep:
         import torch
         self.torch = torch
         self.fmt = fmt
-        self.format = _lib.W4_FMT_NF4 if fmt == "nf4" else _lib.W4_FMT_INT4
-        self.bs = blocksize or (64 if fmt == "nf4" else 128)
+        self.format = {"nf4": _lib.W4_FMT_NF4, "int4": _lib.W4_FMT_INT4, "fp4": _lib.W4_FMT_FP4}[fmt]
+        self.bs = blocksize or {"nf4": 64, "int4": 128, "fp4": 32}[fmt]
         self.M = batch
         self.dev = torch.device(device)
         self.outlier_frac = outlier_frac
@@ -88,7 +88,8 @@ class DecodeStep:
                 w4.check(w4.w4_quantize_nf4(W, packed, sc, self.code, n, k, self.bs), f"quantize {proj}")
             else:
                 sc = torch.empty((n, k // self.bs), dtype=torch.float16, device=self.dev)
-                w4.check(w4.w4_quantize_int4(W, packed, sc, n, k, self.bs), f"quantize {proj}")
+                quant = w4.w4_quantize_int4 if self.format == _lib.W4_FMT_INT4 else w4.w4_quantize_fp4
+                w4.check(quant(W, packed, sc, n, k, self.bs), f"quantize {proj}")
             self.packed.append(packed)
             self.scales.append(sc)
             del W
@@ -158,7 +159,7 @@ def _main():
     import argparse
     import torch
     ap = argparse.ArgumentParser(description=__doc__)
-    ap.add_argument("--fmt", default="nf4", choices=["nf4", "int4"])
+    ap.add_argument("--fmt", default="nf4", choices=["nf4", "int4", "fp4"])
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--layers", type=int, default=synth.N_LAYERS)
     ap.add_argument("--no-lm-head", action="store_true")
