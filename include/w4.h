@@ -251,9 +251,9 @@ int w4_step_destroy(w4_step* step);
  * clears the counters it uses (an asynchronous copy from pageable host memory and a memset on
  * `stream`), then launches; it never calls cudaMalloc, cudaFree or any allocating routine.  The
  * first call on a device looks up the arrays' device addresses (cudaGetSymbolAddress) with that
- * device current and keeps them for the life of the process; make that first call before any
- * stream capture, and do not call this entry point after cudaDeviceReset on that device (the
- * kept addresses belong to the context the reset destroyed).  Every call uses the same arrays,
+ * device current and keeps them, with the id of the device's context; a later call in another
+ * context (after cudaDeviceReset) looks them up again.  Make the first call in a context before
+ * any stream capture.  Every call uses the same arrays,
  * so calls that overlap on the GPU (other streams, other host threads) race and give wrong
  * results: serialise them. */
 #define W4_NOALLOC_MAX_LEVELS 256

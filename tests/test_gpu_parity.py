@@ -366,3 +366,54 @@ def test_tensor_core_timeout_is_reported_and_context_survives(dev, n, k):
     rows = np.unique(np.concatenate([[0, n - 1], np.random.default_rng(n).integers(0, n, 64)]))
     y = gpu_gemv("nf4", packed, sc, x, n, k, bs, dev).cpu().numpy()
     assert_gemv_close(y[:, rows], oracle_gemv("nf4", p_ref, s_ref, x, bs, rows=rows))
+
+
+# ----------------------------------------------------------------------------- precision conditions
+@pytest.mark.parametrize("fmt", ["nf4", "int4", "fp4"])
+@pytest.mark.parametrize("m", [1, 8])
+def test_small_batch_small_magnitude_blocks(dev, fmt, m):
+    """Batches 1 ... 8 carry the block scale in FP32 (NF4) or as the stored FP16 scale, applied to
+    the FP32 partial sums: blocks far below the FP16 normal range (absmax about 5e-6) still meet the
+    bar.  x is scaled by 64 (exact in FP16) so that y stays in the FP16 normal range."""
+    bs = BS[fmt]
+    n, k = 300, 1536
+    w = (synth.weights(9100 + m, n, k) * np.float32(1e-4)).astype(np.float32)
+    x = (synth.activations(9101 + m, m, k).astype(np.float32) * 64).astype(np.float16)
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    if fmt == "nf4":
+        assert float(s_ref.max()) < 6.1e-5                      # every block below the FP16 normal range
+    y = gpu_gemv(fmt, _t(p_ref, dev), _t(s_ref, dev), x, n, k, bs, dev)
+    assert_gemv_close(y.cpu().numpy(), oracle_gemv(fmt, p_ref, s_ref, x, bs))
+
+
+@pytest.mark.parametrize("m", [16, 64])
+def test_tensor_core_nf4_absmax_at_the_low_end_of_the_stated_range(dev, m):
+    """The tcgen05 path rounds the NF4 absmax to FP16: blocks with absmax just above the FP16 normal
+    minimum (6.1e-5) meet the bar."""
+    n, k, bs = 640, 1536, 64
+    w = (synth.weights(9200 + m, n, k) * np.float32(4e-3)).astype(np.float32)
+    x = (synth.activations(9201 + m, m, k).astype(np.float32) * 16).astype(np.float16)
+    p_ref, s_ref = oracle_quantize("nf4", w, bs)
+    assert float(s_ref.min()) >= 6.1e-5 and float(s_ref.max()) < 1e-3
+    st, plan = w4.w4_gemv_plan(w4.W4_FMT_NF4, m, n, k, bs, 152)
+    assert st == 0 and plan["kernel"] == w4.W4_KERNEL_TCGEN05
+    y = gpu_gemv("nf4", _t(p_ref, dev), _t(s_ref, dev), x, n, k, bs, dev)
+    assert_gemv_close(y.cpu().numpy(), oracle_gemv("nf4", p_ref, s_ref, x, bs))
+
+
+@pytest.mark.parametrize("fmt", ["nf4", "int4", "fp4"])
+@pytest.mark.parametrize("m", [1, 8, 16, 64])
+def test_activation_outliers_at_100_sigma(dev, fmt, m):
+    """0.1 % of the activations at +-100 (100 sigma of the N(0, 1) draws), the rest ordinary: every
+    path (small-batch kernel, tcgen05) meets the bar."""
+    bs = BS[fmt]
+    n, k = 512, 1536
+    w = synth.weights(9300 + m, n, k, outlier_frac=0.001)
+    x = synth.activations(9301 + m, m, k).astype(np.float32)
+    rng = np.random.default_rng(9302 + m)
+    idx = rng.choice(m * k, size=max(1, round(0.001 * m * k)), replace=False)
+    x.ravel()[idx] = np.where(rng.random(len(idx)) < 0.5, -100.0, 100.0)
+    x = x.astype(np.float16)
+    p_ref, s_ref = oracle_quantize(fmt, w, bs)
+    y = gpu_gemv(fmt, _t(p_ref, dev), _t(s_ref, dev), x, n, k, bs, dev)
+    assert_gemv_close(y.cpu().numpy(), oracle_gemv(fmt, p_ref, s_ref, x, bs))

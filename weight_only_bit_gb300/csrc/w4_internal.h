@@ -1,6 +1,7 @@
 // w4_internal.h -- host-side declarations shared by libw4's translation units (not installed).
 #pragma once
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -68,6 +69,30 @@ int device_sm_count();
 // cannot encode it (base not 16-byte aligned, row bytes not a multiple of 16, ...).
 bool encode_tmap_2d(CUtensorMap* m, int es, const void* base, long long cols, long long rows, int box_cols,
                     int box_rows);
+
+// Unique id of the CUDA context current on this thread (the runtime's primary context of the current
+// device; a new id after cudaDeviceReset), or 0 if the driver cannot say.
+unsigned long long current_context_id();
+
+// One-time set-up of a kernel's attributes (shared-memory size and the like), repeated for each
+// device and again if that device's context changes (attributes do not survive cudaDeviceReset).
+// One instance per kernel instantiation.
+struct FuncAttrCache {
+  static constexpr int kDevices = 64;
+  std::mutex mu;
+  unsigned long long ctx[kDevices] = {};
+  template <class F>
+  cudaError_t ensure(F&& set_attrs) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
+    const unsigned long long c = current_context_id();
+    std::lock_guard<std::mutex> lock(mu);
+    if (c != 0 && ctx[dev] == c) return cudaSuccess;
+    const cudaError_t e = set_attrs();
+    if (e == cudaSuccess) ctx[dev] = c;
+    return e;
+  }
+};
 
 // Each translation unit's device error word (see w4_common.cuh), read and cleared on the current
 // device: the CUDA-core kernels' and the tcgen05 kernel's.

@@ -731,26 +731,12 @@ static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* 
   return cudaSuccess;
 }
 
-// Per-device, per-kernel-instance launch set-up (the shared-memory attribute), done once.
-struct KernelSetup {
-  std::mutex mu;
-  bool attr_done[kMaxDevices] = {};
-};
-
 template <int KB, bool SC32>
 static cudaError_t launch_prepared(Prepared& P, unsigned* counters, bool pdl, cudaStream_t stream) {
   auto kern = w4_persistent_kernel<KB, SC32>;
-  static KernelSetup setup;   // one per instance
-  const int dev = current_device();
-  if (dev < 0) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lock(setup.mu);
-    if (!setup.attr_done[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap);
-      if (e != cudaSuccess) return e;
-      setup.attr_done[dev] = true;
-    }
-  }
+  static FuncAttrCache attrs;   // one per instance
+  cudaError_t ea = attrs.ensure([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap); });
+  if (ea != cudaSuccess) return ea;
   PParams& p = P.p;
   if (p.nlevels > 1 && !counters) return cudaErrorInvalidValue;
   if (p.ngemvs > 1 && (!p.lvt || !p.gmt)) return cudaErrorInvalidValue;
@@ -845,11 +831,15 @@ static __device__ __align__(128) uint4 g_noalloc_tables[kNoAllocTableBytes / 16]
 static cudaError_t noalloc_arrays(unsigned** counters, void** tables) {
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
+  // the addresses belong to the context they were looked up in: look them up again when the
+  // device's context has changed (cudaDeviceReset)
+  const unsigned long long ctx = current_context_id();
   static std::mutex mu;
   static unsigned* caddr[kMaxDevices] = {};
   static void* taddr[kMaxDevices] = {};
+  static unsigned long long cid[kMaxDevices] = {};
   std::lock_guard<std::mutex> lock(mu);
-  if (caddr[dev] == nullptr) {
+  if (caddr[dev] == nullptr || ctx == 0 || cid[dev] != ctx) {
     void* pc = nullptr;
     void* pt = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&pc, g_noalloc_counters);   // with this device current
@@ -858,6 +848,7 @@ static cudaError_t noalloc_arrays(unsigned** counters, void** tables) {
     if (e != cudaSuccess) return e;
     caddr[dev] = static_cast<unsigned*>(pc);
     taddr[dev] = pt;
+    cid[dev] = ctx;
   }
   *counters = caddr[dev];
   *tables = taddr[dev];

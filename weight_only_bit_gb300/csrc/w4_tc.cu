@@ -264,14 +264,13 @@ static cudaError_t launch_tc_nt(const TcParams& p0, bool pdl, cudaStream_t strea
   const size_t xbytes = 2 * (size_t)(NT * 8) * XS * sizeof(__half);
   const size_t pbytes = (size_t)kTcRows * (NT * 8 + 1) * sizeof(float);
   const size_t smem = kLutBytes + (xbytes > pbytes ? xbytes : pbytes);
-  static bool attr_done = false;
-  if (!attr_done) {
+  static FuncAttrCache attrs;
+  cudaError_t ea = attrs.ensure([&] {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    return e;
+  });
+  if (ea != cudaSuccess) return ea;
   const int nrb = (p.N + kTcRows - 1) / kTcRows;
   // K split: enough CTAs to cover the SMs, at most 8 (a portable cluster) and one window each
   int ks = (device_sm_count() + nrb - 1) / nrb;

@@ -606,12 +606,9 @@ bool plan_tc5(int M, int N, int K, int bs, int sms, Tc5Plan* o) {
 template <int FMT, int NB>
 static cudaError_t launch_tc5_nb(T5Params& p, const Tc5Plan& pl, bool pdl, cudaStream_t stream) {
   auto kern = w4_tc5_kernel<FMT, NB>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static FuncAttrCache attrs;
+  cudaError_t ea = attrs.ensure([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024); });
+  if (ea != cudaSuccess) return ea;
   if (!encode_tmap_2d(&p.tm_x, 2, p.tm_x_base, p.K, p.M, kT5Kc, NB))
     return cudaErrorNotSupported;
   p.np = pl.np;

@@ -1,4 +1,5 @@
-// w4_tmap.cu -- host-side encoding of the TMA tensor maps the kernels copy tiles with.
+// w4_tmap.cu -- driver entry points the library uses (looked up through the runtime, so there is no
+// link against libcuda): the TMA tensor-map encoder and the current context's id.
 #include <mutex>
 
 #include <cuda.h>
@@ -24,6 +25,31 @@ static EncodeFn encoder() {
       fn = reinterpret_cast<EncodeFn>(f);
   });
   return fn;
+}
+
+using CtxCurrentFn = CUresult (*)(CUcontext*);
+using CtxIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+unsigned long long current_context_id() {
+  static CtxCurrentFn cur = nullptr;
+  static CtxIdFn id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      cur = reinterpret_cast<CtxCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      id = reinterpret_cast<CtxIdFn>(f);
+  });
+  if (!cur || !id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long v = 0;
+  if (cur(&c) != CUDA_SUCCESS || c == nullptr || id(c, &v) != CUDA_SUCCESS) return 0;
+  return v;
 }
 
 bool encode_tmap_2d(CUtensorMap* m, int es, const void* base, long long cols, long long rows, int box_cols,
