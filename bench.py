@@ -32,6 +32,8 @@ WORKLOAD = ("Qwen2.5-1.5B-shaped decode step, batch 1: 197 NF4 GEMVs (28 layers 
             "k 256x1536, v 256x1536, o 1536x1536, gate 8960x1536, up 8960x1536, down 1536x8960, "
             "+ lm_head 151936x1536), blocksize 64, FP32 absmax, weights N(0,0.02), x N(0,1) FP16")
 FALLBACK_HBM_GBS = 6800.0
+BLOCK = {"nf4": 64, "int4": 128, "fp4": 32}          # default block / group size per format
+FORMAT_ID = {"nf4": 0, "int4": 1, "fp4": 2}          # w4_format of include/w4.h
 
 
 def peaks():
@@ -53,8 +55,8 @@ def bf16_peak():
 
 def run_sweep(args):
     """The batch sweep of the pages' small-batch configurations: every decode shape alone at batch
-    1, 8, 32 and 128, NF4 and INT4, weights N(0, 0.02) with 0.1 % outliers at 10 sigma.  One JSON
-    line; not part of the default run."""
+    1, 8, 32 and 128, NF4, INT4 and FP4, weights N(0, 0.02) with 0.1 % outliers at 10 sigma.  One
+    JSON line; not part of the default run."""
     import torch
     from weight_only_bit_gb300 import build as _b
     _b.build()
@@ -72,7 +74,7 @@ def run_sweep(args):
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("w4_persist.cu", "w4_decode.cuh", "w4_common.cuh"):
+    for f in ("w4_persist.cu", "w4_mma_unit.cuh", "w4_decode.cuh", "w4_common.cuh"):
         h.update(open(os.path.join(ROOT, "weight_only_bit_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -308,7 +310,7 @@ def per_shape(fmt, dev, torch, hbm, M=1, tflops_peak=None, outlier_frac=0.0, onl
     import weight_only_bit_gb300 as w4
     from weight_only_bit_gb300 import synth
     from weight_only_bit_gb300 import _lib
-    bs = 64 if fmt == "nf4" else 128
+    bs = BLOCK[fmt]
     out = {}
     code = None
     if fmt == "nf4":
@@ -325,8 +327,10 @@ def per_shape(fmt, dev, torch, hbm, M=1, tflops_peak=None, outlier_frac=0.0, onl
         sc = torch.empty((n, k // bs), dtype=sdt, device=dev)
         if fmt == "nf4":
             w4.check(w4.w4_quantize_nf4(W, packed, sc, code, n, k, bs))
-        else:
+        elif fmt == "int4":
             w4.check(w4.w4_quantize_int4(W, packed, sc, n, k, bs))
+        else:
+            w4.check(w4.w4_quantize_fp4(W, packed, sc, n, k, bs))
         del W
         per = n * k // 2 + sc.numel() * sc.element_size()
         copies = max(2, min(4096, (4 * 129 * 2 ** 20) // per + 1))
@@ -334,7 +338,7 @@ def per_shape(fmt, dev, torch, hbm, M=1, tflops_peak=None, outlier_frac=0.0, onl
         S = sc.reshape(1, -1).repeat(copies, 1)
         x = torch.from_numpy(synth.activations(synth.x_seed(0, synth.X_SLOT[name], M), M, k)).to(dev)
         y = torch.empty((M, n), dtype=torch.float16, device=dev)
-        descs = [dict(format=_lib.W4_FMT_NF4 if fmt == "nf4" else _lib.W4_FMT_INT4, packed=P[i], scales=S[i],
+        descs = [dict(format=FORMAT_ID[fmt], packed=P[i], scales=S[i],
                       codebook=code, x=x, y=y, M=M, N=n, K=k, blocksize=bs) for i in range(copies)]
         arr = w4._descs(descs)
         lib = w4.lib()
@@ -470,18 +474,32 @@ def run_ours(args):
                                          "GB_s": round(nbytes / (ms_c * 1e-3) / 1e9, 1),
                                          "frac_of_measured": round(nbytes / (ms_c * 1e-3) / 1e9 / hbm, 4),
                                          "launches_per_step": nlaunch}
-        # INT4 step (same shapes, grouped levels) and each shape alone
-        s4 = DecodeStep("int4", batch=1, device=str(dev), levels="grouped").build().capture()
-        ms4 = time_graph(s4, stream, nrep, args.warmup, torch)
-        b4 = s4.bytes_per_step()
-        extra["int4_step"] = {"us": round(ms4 * 1e3, 2), "GB_s": round(b4 / (ms4 * 1e-3) / 1e9, 1),
-                              "frac_of_measured": round(b4 / (ms4 * 1e-3) / 1e9 / hbm, 4), "bytes": b4}
-        s4.close()
-        del s4
-        torch.cuda.empty_cache()
+        # the other formats' steps at batch 1, and the small batches of the decode step (same
+        # shapes, grouped levels, one persistent launch each)
+        for tag, fmt, batch in (("int4_step", "int4", 1), ("fp4_step", "fp4", 1), ("nf4_step_b4", "nf4", 4),
+                                ("nf4_step_b8", "nf4", 8), ("int4_step_b8", "int4", 8)):
+            s4 = DecodeStep(fmt, batch=batch, device=str(dev), levels="grouped").build().capture()
+            ms4 = time_graph(s4, stream, nrep, args.warmup, torch)
+            b4 = s4.bytes_per_step()
+            extra[tag] = {"us": round(ms4 * 1e3, 2), "GB_s": round(b4 / (ms4 * 1e-3) / 1e9, 1),
+                          "frac_of_measured": round(b4 / (ms4 * 1e-3) / 1e9 / hbm, 4), "bytes": b4,
+                          "batch": batch, "format": fmt, "group": BLOCK[fmt]}
+            s4.close()
+            del s4
+            torch.cuda.empty_cache()
         shapes, weighted = per_shape("nf4", dev, torch, hbm)
         extra["per_shape_nf4"] = shapes
         extra["weighted_step_us_nf4"] = round(weighted, 2)
+        # the small-shape configuration: NF4 256 x 1536 at batch 1 (the k / v projection)
+        extra["c1_nf4_256x1536_b1"] = shapes["k"]
+        # small batches on gate, down and q (NF4 and INT4, batch 8 and 32)
+        c4 = {}
+        tfp, _ = bf16_peak()
+        for fmt in ("nf4", "int4"):
+            for M in (8, 32):
+                sh, _ = per_shape(fmt, dev, torch, hbm, M=M, tflops_peak=tfp, only={"gate", "down", "q"})
+                c4[f"{fmt}_b{M}"] = sh
+        extra["c4_small_batches"] = c4
         # read-only streaming ceiling: a library reduction reading a 2 GiB buffer once per pass
         buf = torch.ones(1 << 29, dtype=torch.float32, device=dev)
         with torch.cuda.stream(stream):
@@ -545,7 +563,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip the INT4 step and the per-shape table")
     ap.add_argument("--sweep", action="store_true", help="only the per-shape batch sweep (1, 8, 32, 128; NF4, INT4)")
     ap.add_argument("--sweep-batches", default="1,8,32,128", help="batches of the sweep, comma-separated")
-    ap.add_argument("--sweep-formats", default="nf4,int4", help="formats of the sweep, comma-separated")
+    ap.add_argument("--sweep-formats", default="nf4,int4,fp4", help="formats of the sweep, comma-separated")
     ap.add_argument("--sweep-shapes", default="", help="decode shapes of the sweep (default: all), comma-separated")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -36,16 +36,17 @@
 //     (a box of 128 bytes x the tile's rows, 128-byte swizzled: the 16-byte chunk c of tile row r
 //     lands at chunk c ^ (r & 7), so the fragment loads of a warp hit distinct banks) and its scales
 //     with one 1-D bulk copy, completion on the stage's mbarrier.  Weights never depend on other
-//     GEMVs, so it runs ahead across level boundaries.  Copies other than a level's first tile are
-//     issued only while the CTA's consumers compute (a stream gate opened once a level starts and
-//     closed before the stage of the CTA's last tile of the level is released), because data
-//     arriving at the SM while a level's completion is published and the next level waits slows
-//     that release and its polls; the first tile of a level is never held back, since the
-//     consumers wait for it before they wait for the previous level;
+//     GEMVs, so it runs ahead across level boundaries.  Copies are issued only while the CTA's
+//     consumers compute (a stream gate opened once a level starts and closed before the stage of
+//     the CTA's last tile of the level is released), because data arriving at the SM while a
+//     level's completion is published and the next level waits slows that release and its polls.
+//     The consumers open the gate before they wait for a level's first tile, so a tile held back
+//     at a level's end is issued as soon as the level starts;
 //   * 14 consumer warps (16 warps in all, so each thread may hold 128 registers): the units of each tile, round-robin over the warps (continuing across
 //     tiles, so an uneven tile does not always load the same warps);
 //   * reducer warp: sums each row's partials, writes y, and after the CTA's last tile of a level
-//     publishes completion with one release.
+//     publishes completion with one release, before it reads any table entry of the next tile
+//     (whether a tile ends the CTA's part of a level is known from the cursor alone).
 // Every wait is bounded in wall-clock time; a lost wait is recorded in the device error word and
 // the kernel runs to its end without further waiting.
 #include <cstdint>
@@ -101,7 +102,9 @@ struct PGemv {
 static_assert(sizeof(PGemv) % 16 == 0, "PGemv is read as 16-byte vectors");
 
 struct PLevel {
-  int gemv0, ngemv, tile0, ntiles;
+  int gemv0;
+  int wait;                // releases this level waits for: the CTAs owning tiles of the level before
+  int tile0, ntiles;
 };
 
 // Launch parameters.  A single-GEMV launch carries its level, GEMV and tensor map here; a
@@ -214,28 +217,33 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
 }
 
 
-// The tiles of one CTA, in order across levels: level, GEMV and global tile index (with the end
-// tiles of the current level and GEMV kept, so that a step reads the tables only when it moves on).
+// The tiles of one CTA, in order across levels: level, GEMV (index and descriptor) and global tile
+// index, with the end tiles of the current level and GEMV kept, so that a step reads the tables
+// only when it moves on and "is this the CTA's last tile of its level" needs no table read.
 struct TileCursor {
-  int L, g, t, lend, gend;
+  int L, g, t, lend, gend, wait;
+  PGemv gm;
   __device__ __forceinline__ void start(const PParams& p) {
     L = 0;
     seek(p);
   }
   __device__ __forceinline__ void find_gemv(const PParams& p) {
     for (;;) {
-      const PGemv gm = gemv_at(p, g);
+      gm = gemv_at(p, g);
       gend = gm.tile0 + gm.ntiles;
       if (t < gend) break;
       ++g;
     }
   }
+  // this is the CTA's last tile of level L (the next one, if any, belongs to a later level)
+  __device__ __forceinline__ bool level_last() const { return t + (int)gridDim.x >= lend; }
   // from level L on: this CTA's first tile of the first level that has one
   __device__ __forceinline__ void seek(const PParams& p) {
     while (L < p.nlevels) {
       const PLevel lv = level_at(p, L);
       t = first_owned(lv.tile0);
       lend = lv.tile0 + lv.ntiles;
+      wait = lv.wait;
       if (t < lend) {
         g = lv.gemv0;
         find_gemv(p);
@@ -298,20 +306,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
     TileCursor cur;
     cur.start(p);
     int j = 0;
-    int prev_level = -1;
     bool ok = true;
     for (; cur.valid(p); cur.next(p), ++j) {
-      const PGemv gm = gemv_at(p, cur.g);
+      const PGemv& gm = cur.gm;
       const int st = j % NS;
       const int round = j / NS;
       // Copies of the first NS tiles may overlap the previous kernel in the stream; the bounded
       // waits start only once that kernel is complete.
       if (round == 1 && st == 0) pdl_wait();
       if (lane == 0 && round > 0 && ok) ok = mbar_wait(&empty[st], (round - 1) & 1, 0x201);
-      // the gate holds back every tile but the first of a level: the consumers wait for that one
-      // before they wait for the previous level (and reopen the gate)
-      if (lane == 0 && ok && cur.L == prev_level) ok = wait_gate(gate, 0x20a);
-      prev_level = cur.L;
+      if (lane == 0 && ok) ok = wait_gate(gate, 0x20a);
       if (lane == 0 && NS > kMaxInFlight && j >= kMaxInFlight && ok) {
         const int jd = j - kMaxInFlight;
         ok = mbar_wait(&full[jd % NS], (jd / NS) & 1, 0x209);
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
     bool ok = true;
     for (; cur.valid(p); ++j) {
       const int L = cur.L;
-      const PGemv gm = gemv_at(p, cur.g);
+      const PGemv& gm = cur.gm;
       const int t = cur.t;
       const int b = j % kRedBufs;
       if (ok) ok = mbar_wait(&rfull[b], (j / kRedBufs) & 1, 0x203);
@@ -374,13 +378,14 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
         const int m = o / nrows;
         gm.y[(size_t)m * gm.N + r0 + (o - m * nrows)] = __float2half_rn(v);
       }
-      cur.next(p);
-      const bool publish = p.counters && cur.L != L;   // this CTA's last tile of level L
+      // the CTA's last tile of level L: publish before the cursor reads the next tile's tables
+      const bool publish = p.counters && cur.level_last();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&rfree[b]);
         if (publish) red_release_add(&p.counters[L], 1u);
       }
+      cur.next(p);
     }
     // end of the launch: the last CTA to finish resets the counters for the next launch
     asm volatile("bar.sync 2, %0;" ::"r"(n_cons + 32) : "memory");
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
   int Lcur = -1;
   for (; cur.valid(p); cur.next(p), ++j) {
     const int L = cur.L;
-    const PGemv gm = gemv_at(p, cur.g);
+    const PGemv& gm = cur.gm;
     const int st = j % NS;
     const int b = j % kRedBufs;
     const int r0 = (cur.t - gm.tile0) * gm.rpt;
@@ -445,24 +450,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
     const int u0 = (warp - ubase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
     int rg = u0 / gm.nspan, c = u0 - rg * gm.nspan;
     const int rsub_a = KB == 64 ? 2 * g : g, rsub_b = rsub_a + (KB == 64 ? 1 : 8);
-    bool is_level_end;
-    {
-      TileCursor nx = cur;
-      nx.next(p);
-      is_level_end = nx.L != L && nx.L < p.nlevels;
-    }
+    const bool is_level_end = cur.level_last() && L + 1 < p.nlevels;
     if (L != Lcur) {
-      // ---- this CTA's first tile of the level: its weights are in (the producer never holds the
-      // first tile of a level back), then wait until this level's inputs exist
-      if (ok) ok = mbar_wait(&full[st], (j / NS) & 1, 0x205);
+      // ---- this CTA's first tile of the level: wait until this level's inputs exist
       if (!pdl_done) {
         pdl_wait();
         pdl_done = true;
       }
       if (L > 0 && p.counters) {
         // every CTA that owns a tile of level L-1 adds one when it has finished them all
-        const unsigned owners = (unsigned)min(G, level_at(p, L - 1).ntiles);
-        if (tid == 0 && ok) ok = wait_counter(&p.counters[L - 1], owners, 0x204);
+        if (tid == 0 && ok) ok = wait_counter(&p.counters[L - 1], (unsigned)cur.wait, 0x204);
       }
       // the level's start for all consumers: thread 0's acquire orders every consumer's reads of
       // x after the previous level's writes
@@ -702,7 +699,7 @@ static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* 
     }
     PLevel& lv = P.lv[(size_t)Lv];
     lv.gemv0 = first;
-    lv.ngemv = i - first;
+    lv.wait = Lv > 0 ? min(gmax, P.lv[(size_t)Lv - 1].ntiles) : 0;
     lv.tile0 = tile;
     const long long tpc = (rows + (long long)gmax * rmin - 1) / ((long long)gmax * rmin);
     for (int q = first; q < i; ++q) {
