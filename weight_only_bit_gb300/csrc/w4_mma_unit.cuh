@@ -108,8 +108,8 @@ __device__ __forceinline__ void span_scales(float (&sk)[kSpanK / KB], uint32_t a
 // row of MMA row g and of MMA row g + 8 (128 bytes each); off0[j], off1[j]: this lane's byte offset
 // of k block j in those swizzled rows; s0a, s1a: their scale rows (at the span's first scale); v0 /
 // v1 false for rows beyond the tile (their scales are zeroed); xg: this lane's x elements of the
-// span, loaded only where xok (batch row g exists; columns at or above the batch are never
-// stored).  NSC > 0: the span is full and its NSC scales per row are one aligned vector (K a
+// span (lanes whose batch row g is at or above the batch read the last batch row instead: their
+// MMA columns are never stored).  NSC > 0: the span is full and its NSC scales per row are one aligned vector (K a
 // multiple of 128); NSC == 0: the general case, nkb k blocks present, scale index of block j =
 // sidx0 + (j >> sshift) relative to s0a / s1a.
 // KB = 64: per 64-k block, 8 packed bytes per lane per row and 4 MMAs; KB = 32: 4 bytes, 2 MMAs.
@@ -117,7 +117,7 @@ __device__ __forceinline__ void span_scales(float (&sk)[kSpanK / KB], uint32_t a
 template <int KB, bool SC32, int NSC>
 __device__ __forceinline__ void mma_unit(float (&acc)[4], uint32_t a0, uint32_t a1, const uint32_t (&off0)[kSpanK / KB],
                                          const uint32_t (&off1)[kSpanK / KB], uint32_t s0a, uint32_t s1a,
-                                         bool v0, bool v1, const uint8_t* xg, bool xok, int sidx0, int sshift, int nkb,
+                                         bool v0, bool v1, const uint8_t* xg, int sidx0, int sshift, int nkb,
                                          uint32_t lut_lane, int lane) {
   constexpr int NKB = kSpanK / KB;     // k blocks per full span
   constexpr int RUN = KB / 8;          // packed bytes per lane per row per k block
@@ -132,7 +132,7 @@ __device__ __forceinline__ void mma_unit(float (&acc)[4], uint32_t a0, uint32_t 
 #pragma unroll
     for (int q = 0; q < KB / 32; ++q) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (xok && (FULL || j < nkb)) v = ld_x_v4(xg + j * (KB * 2) + 16 * q);
+      if (FULL || j < nkb) v = ld_x_v4(xg + j * (KB * 2) + 16 * q);
       xr[j][4 * q + 0] = v.x; xr[j][4 * q + 1] = v.y; xr[j][4 * q + 2] = v.z; xr[j][4 * q + 3] = v.w;
     }
   }

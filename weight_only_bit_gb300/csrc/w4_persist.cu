@@ -267,7 +267,9 @@ struct TileCursor {
   }
 };
 
-template <int KB, bool SC32>
+// NSCF: the number of block scales per full span when every GEMV of the launch has the same block
+// size (1, 2 or 4), compiled in; 0 when they differ (the general unit serves every span).
+template <int KB, bool SC32, int NSCF>
 __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid_constant__ PParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -442,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
     const uint32_t tile_s = smem_u32(smem + Lo.w + st * p.stage_w);
     const uint32_t stile_s = smem_u32(smem + Lo.s + st * p.stage_s);
     float* red = red_base + b * p.red_floats;
-    // x of batch row g, in lanes whose batch row exists (the others' B columns are never stored)
-    const bool xok = g < p.M;
+    // x of batch row g (the last batch row in lanes above the batch: those B columns are never
+    // stored)
     const uint8_t* xrow = reinterpret_cast<const uint8_t*>(gm.x + (size_t)min(g, p.M - 1) * gm.K) + (KB / 2) * tq;
     // this warp's units u = u0, u0 + 14, ... of the tile as (row group rg, span c), stepped without
     // divisions; MMA rows g and g + 8 stand for tile rows ra and rb of the row group
@@ -486,20 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
         const int sidx0 = (c * kSpanK) >> lgbs;
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         const bool v0 = ra < nrows, v1 = rb < nrows;
-        if (full_last) {
-          // every span full, each row's span scales one aligned vector: max(1, 128 / bs) of them
+        if (NSCF > 0 && full_last) {
+          // every span full, each row's span scales one aligned vector: NSCF = max(1, 128 / bs)
           const uint32_t so = (uint32_t)(sidx0 * (SC32 ? 4 : 2));
-          if (KB == 32) {
-            if (lgbs == 5) mma_unit<KB, SC32, 4>(acc, a0, a1, o0, o1, s0a + so, s1a + so, v0, v1, xg, xok, 0, 0, 0, lut_lane, lane);
-            else mma_unit<KB, SC32, 0>(acc, a0, a1, o0, o1, s0a, s1a, v0, v1, xg, xok, sidx0, sshift, kSpanK / KB, lut_lane, lane);
-          } else if (lgbs == 6) {
-            mma_unit<KB, SC32, 2>(acc, a0, a1, o0, o1, s0a + so, s1a + so, v0, v1, xg, xok, 0, 0, 0, lut_lane, lane);
-          } else {
-            mma_unit<KB, SC32, 1>(acc, a0, a1, o0, o1, s0a + so, s1a + so, v0, v1, xg, xok, 0, 0, 0, lut_lane, lane);
-          }
+          mma_unit<KB, SC32, NSCF>(acc, a0, a1, o0, o1, s0a + so, s1a + so, v0, v1, xg, 0, 0, 0, lut_lane, lane);
         } else {
           const int nkb = min(kSpanK, gm.K - c * kSpanK) / KB;
-          mma_unit<KB, SC32, 0>(acc, a0, a1, o0, o1, s0a, s1a, v0, v1, xg, xok, sidx0, sshift, nkb, lut_lane, lane);
+          mma_unit<KB, SC32, 0>(acc, a0, a1, o0, o1, s0a, s1a, v0, v1, xg, sidx0, sshift, nkb, lut_lane, lane);
         }
         // partials: batch rows 2t, 2t + 1 of weight rows ra and rb
 #pragma unroll
@@ -728,9 +723,9 @@ static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* 
   return cudaSuccess;
 }
 
-template <int KB, bool SC32>
+template <int KB, bool SC32, int NSCF>
 static cudaError_t launch_prepared(Prepared& P, unsigned* counters, bool pdl, cudaStream_t stream) {
-  auto kern = w4_persistent_kernel<KB, SC32>;
+  auto kern = w4_persistent_kernel<KB, SC32, NSCF>;
   static FuncAttrCache attrs;   // one per instance
   cudaError_t ea = attrs.ensure([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap); });
   if (ea != cudaSuccess) return ea;
@@ -754,14 +749,25 @@ static cudaError_t launch_prepared(Prepared& P, unsigned* counters, bool pdl, cu
   return e;
 }
 
+// The instance for the launch's format, k-block width and scales per span (0 when the GEMVs' block
+// sizes differ).
 static cudaError_t dispatch(int fmt, Prepared& P, unsigned* counters, bool pdl, cudaStream_t s) {
-  const bool kb64 = P.plan.kb == 64;
-  if (fmt == 0) {
-    if (kb64) return launch_prepared<64, true>(P, counters, pdl, s);
-    return launch_prepared<32, true>(P, counters, pdl, s);
+  int bs = P.gm[0].bs;
+  for (const PGemv& g : P.gm)
+    if (g.bs != bs) bs = 0;
+  const int nsc = bs == 0 ? 0 : (bs >= kSpanK ? 1 : kSpanK / bs);
+  if (P.plan.kb == 32) {   // block size 32: four scales per span
+    if (fmt == 0) return launch_prepared<32, true, 4>(P, counters, pdl, s);
+    return launch_prepared<32, false, 4>(P, counters, pdl, s);
   }
-  if (kb64) return launch_prepared<64, false>(P, counters, pdl, s);
-  return launch_prepared<32, false>(P, counters, pdl, s);
+  if (fmt == 0) {
+    if (nsc == 2) return launch_prepared<64, true, 2>(P, counters, pdl, s);
+    if (nsc == 1) return launch_prepared<64, true, 1>(P, counters, pdl, s);
+    return launch_prepared<64, true, 0>(P, counters, pdl, s);
+  }
+  if (nsc == 2) return launch_prepared<64, false, 2>(P, counters, pdl, s);
+  if (nsc == 1) return launch_prepared<64, false, 1>(P, counters, pdl, s);
+  return launch_prepared<64, false, 0>(P, counters, pdl, s);
 }
 
 cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scales, const float* codebook,
