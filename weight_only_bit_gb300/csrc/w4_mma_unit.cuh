@@ -52,19 +52,69 @@ __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lane, uint32_t w, int 
   return lds_table(lut_lane + (byte << 7));
 }
 
-// Sum of one output's partials rr[0 .. C) in order (16-byte loads; rr 16-byte aligned).
-__device__ __forceinline__ float sum_spans(const float* rr, int C) {
-  float s = 0.0f;
-  int c = 0;
-  for (; c + 4 <= C; c += 4) {
-    const float4 v = *reinterpret_cast<const float4*>(rr + c);
-    s += v.x;
-    s += v.y;
-    s += v.z;
-    s += v.w;
+// Sum of one output's span partials rr[0 .. C) in an order that depends only on C: eight
+// interleaved sequences s_i = rr[i] + rr[i + 8] + ... (each from 0, in index order), then
+// ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7)).  Q consecutive lanes (1, 2, 4 or 8, aligned
+// to Q) share the output: the lane at position sub of its group forms sequences sub, sub + Q, ...
+// and the group combines them with shuffles along the same tree (IEEE addition is commutative,
+// so both lanes of a pair get the same bits).  Every lane of the warp must call it; the result
+// is the same for every Q.
+template <int Q>
+__device__ __forceinline__ float sum_spans(const float* rr, int C, int sub) {
+  constexpr int NK = 8 / Q;
+  float s[NK];
+#pragma unroll
+  for (int k = 0; k < NK; ++k) s[k] = 0.0f;
+  for (int j = 0; j < C; j += 8) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k) {
+      const int i = j + sub + Q * k;
+      if (i < C) s[k] += rr[i];
+    }
   }
-  for (; c < C; ++c) s += rr[c];
-  return s;
+  if (Q >= 2) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k) s[k] += __shfl_xor_sync(0xffffffffu, s[k], 1);
+  }
+  if (Q >= 4) {
+#pragma unroll
+    for (int k = 0; k < NK; ++k) s[k] += __shfl_xor_sync(0xffffffffu, s[k], 2);
+  }
+  if (Q == 8) return s[0] + __shfl_xor_sync(0xffffffffu, s[0], 4);
+  if (Q == 4) return s[0] + s[1];
+  if (Q == 2) return (s[0] + s[1]) + (s[2] + s[3]);
+  return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+}
+
+// The same sum (one lane per output) for R outputs at once, rr[r] the partials of output r: every
+// load of a group of eight spans is issued before the first add, so a pass costs one shared-memory
+// round trip per eight spans for all R outputs (the queue is long while the units decode).
+template <int R>
+__device__ __forceinline__ void sum_spans_batch(float (&out)[R], const float* const (&rr)[R], int C) {
+  float s[R][8];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s[r][k] = 0.0f;
+  }
+  for (int j = 0; j < C; j += 8) {
+    float v[R][8];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[r][k] = j + k < C ? rr[r][j + k] : 0.0f;
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (j + k < C) s[r][k] += v[r][k];
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    out[r] = ((s[r][0] + s[r][1]) + (s[r][2] + s[r][3])) + ((s[r][4] + s[r][5]) + (s[r][6] + s[r][7]));
 }
 
 // Loads the NSC = max(1, 128 / bs) scales of one span of one row (NSC * ES bytes, aligned to that

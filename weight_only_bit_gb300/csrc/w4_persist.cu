@@ -83,9 +83,9 @@ __host__ __device__ constexpr int span_slot(int rows) { return ((rows + 7) / 8) 
 // A stage: the boxes of a tile, then 1 KB that the last row group may read past the last box (its
 // rows beyond the tile are never used).
 __host__ __device__ constexpr int stage_bytes(int nbox, int rows) { return nbox * span_slot(rows) + 1024; }
-// Floats per (batch row, weight row) in a partial-sum buffer: at least the span count and 4 more
-// than a multiple of 8, so that the reducer's 16-byte loads of eight rows hit distinct banks.
-__host__ __device__ constexpr int part_stride(int C) { return C + ((4 - C) & 7); }
+// Floats per (batch row, weight row) in a partial-sum buffer: the span count, made odd, so that the
+// reducer's loads of 32 outputs and the consumers' stores of eight rows hit distinct banks.
+__host__ __device__ constexpr int part_stride(int C) { return C | 1; }
 
 struct PGemv {
   const uint8_t* packed;
@@ -267,6 +267,43 @@ struct TileCursor {
   }
 };
 
+// The reducer's work for one tile with more outputs than lanes: each lane sums R outputs
+// o = base + lane + 32 r at once.
+template <int R>
+__device__ __forceinline__ void reduce_tile_batched(const float* red, const PGemv& gm, int outs, int nrows, int r0,
+                                                    int lane) {
+  for (int base = 0; base < outs; base += 32 * R) {
+    const float* rr[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) rr[r] = red + min(base + lane + 32 * r, outs - 1) * gm.cp;
+    float v[R];
+    sum_spans_batch<R>(v, rr, gm.nspan);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int o = base + lane + 32 * r;
+      if (o < outs) {
+        const int m = o / nrows;
+        gm.y[(size_t)m * gm.N + r0 + (o - m * nrows)] = __float2half_rn(v[r]);
+      }
+    }
+  }
+}
+
+// The reducer's work for one tile: each output o = m * nrows + r (batch row m, tile row r) summed
+// over its spans by Q lanes, written to y as FP16.
+template <int Q>
+__device__ __forceinline__ void reduce_tile(const float* red, const PGemv& gm, int outs, int nrows, int r0,
+                                            int lane) {
+  for (int base = 0; base < outs; base += 32 / Q) {
+    const int o = base + lane / Q;
+    const float v = sum_spans<Q>(red + min(o, outs - 1) * gm.cp, gm.nspan, lane % Q);
+    if (o < outs && lane % Q == 0) {
+      const int m = o / nrows;
+      gm.y[(size_t)m * gm.N + r0 + (o - m * nrows)] = __float2half_rn(v);
+    }
+  }
+}
+
 // NSCF: the number of block scales per full span when every GEMV of the launch has the same block
 // size (1, 2 or 4), compiled in; 0 when they differ (the general unit serves every span).
 template <int KB, bool SC32, int NSCF>
@@ -375,11 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
       const float* red = red_base + b * p.red_floats;
       // output o = m * nrows + r: partials red[o * cp ... + nspan)
       const int outs = nrows * p.M;
-      for (int o = lane; o < outs; o += 32) {
-        const float v = sum_spans(red + o * gm.cp, gm.nspan);
-        const int m = o / nrows;
-        gm.y[(size_t)m * gm.N + r0 + (o - m * nrows)] = __float2half_rn(v);
-      }
+      // as many lanes per output (1, 2, 4 or 8) as make one pass over the tile's outputs
+      if (outs <= 4) reduce_tile<8>(red, gm, outs, nrows, r0, lane);
+      else if (outs <= 8) reduce_tile<4>(red, gm, outs, nrows, r0, lane);
+      else if (outs <= 16) reduce_tile<2>(red, gm, outs, nrows, r0, lane);
+      else reduce_tile_batched<4>(red, gm, outs, nrows, r0, lane);
       // the CTA's last tile of level L: publish before the cursor reads the next tile's tables
       const bool publish = p.counters && cur.level_last();
       __syncwarp();
