@@ -86,9 +86,11 @@ __device__ __forceinline__ float sum_spans(const float* rr, int C, int sub) {
   return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
-// The same sum (one lane per output) for R outputs at once, rr[r] the partials of output r: every
-// load of a group of eight spans is issued before the first add, so a pass costs one shared-memory
-// round trip per eight spans for all R outputs (the queue is long while the units decode).
+// The same sum (one lane per output) for R outputs at once, rr[r] the partials of output r (16-byte
+// aligned; the eight floats of each group of eight spans may be read past C): every load of a
+// group of eight spans is issued before the first add, as two 16-byte loads per output, so a pass
+// costs one shared-memory round trip per eight spans for all R outputs (the queue is long while
+// the units decode).
 template <int R>
 __device__ __forceinline__ void sum_spans_batch(float (&out)[R], const float* const (&rr)[R], int C) {
   float s[R][8];
@@ -98,17 +100,18 @@ __device__ __forceinline__ void sum_spans_batch(float (&out)[R], const float* co
     for (int k = 0; k < 8; ++k) s[r][k] = 0.0f;
   }
   for (int j = 0; j < C; j += 8) {
-    float v[R][8];
+    float4 v[R][2];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) v[r][k] = j + k < C ? rr[r][j + k] : 0.0f;
+      v[r][0] = *reinterpret_cast<const float4*>(rr[r] + j);
+      v[r][1] = *reinterpret_cast<const float4*>(rr[r] + j + 4);
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
+      const float w[8] = {v[r][0].x, v[r][0].y, v[r][0].z, v[r][0].w, v[r][1].x, v[r][1].y, v[r][1].z, v[r][1].w};
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        if (j + k < C) s[r][k] += v[r][k];
+        if (j + k < C) s[r][k] += w[k];
       }
     }
   }

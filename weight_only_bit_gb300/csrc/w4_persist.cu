@@ -83,9 +83,13 @@ __host__ __device__ constexpr int span_slot(int rows) { return ((rows + 7) / 8) 
 // A stage: the boxes of a tile, then 1 KB that the last row group may read past the last box (its
 // rows beyond the tile are never used).
 __host__ __device__ constexpr int stage_bytes(int nbox, int rows) { return nbox * span_slot(rows) + 1024; }
-// Floats per (batch row, weight row) in a partial-sum buffer: the span count, made odd, so that the
-// reducer's loads of 32 outputs and the consumers' stores of eight rows hit distinct banks.
-__host__ __device__ constexpr int part_stride(int C) { return C | 1; }
+// Floats per (batch row, weight row) in a partial-sum buffer: at least the span count and 4 more
+// than a multiple of 8, so rows are 16-byte aligned and the reducer's 16-byte loads of eight
+// consecutive outputs hit distinct banks.
+__host__ __device__ constexpr int part_stride(int C) { return C + ((4 - C) & 7); }
+// Floats a partial-sum buffer holds past its last row: the reducer reads whole groups of eight
+// spans.
+constexpr int kRedSlackFloats = 8;
 
 struct PGemv {
   const uint8_t* packed;
@@ -653,7 +657,7 @@ static bool plan_layout(int fmt, int M, const Job* jobs, int n, Plan& P) {
       P.red_floats = max(P.red_floats, gg.red_need);
     }
     if (!fits) continue;
-    P.red_floats = (P.red_floats + 3) & ~3;
+    P.red_floats = (P.red_floats + kRedSlackFloats + 3) & ~3;
     for (P.stages = kMaxStages; P.stages >= 2; --P.stages) {
       P.L = playout(P.stages, P.stage_w, P.stage_s, P.red_floats);
       if (P.L.total + 1024 <= kSmemCap) return true;   // + the 1 KB alignment slack
