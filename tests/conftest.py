@@ -8,13 +8,20 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built libw4")
-    # a per-test limit where the pytest-timeout plugin is installed (every device wait is bounded, so
-    # a test that runs this long is stuck in a chain of expiring waits, not computing)
-    if config.pluginmanager.hasplugin("timeout") and not getattr(config.option, "timeout", None):
-        config.option.timeout = 600
 
 
 import pytest
+
+
+def pytest_collection_modifyitems(config, items):
+    # a per-test limit where the pytest-timeout plugin is installed (every device wait is bounded, so
+    # a test that runs this long is stuck in a chain of expiring waits, not computing); the thread
+    # method ends the process even while the main thread is blocked inside a CUDA call
+    if not config.pluginmanager.hasplugin("timeout"):
+        return
+    for item in items:
+        if item.get_closest_marker("timeout") is None:
+            item.add_marker(pytest.mark.timeout(300, method="thread"))
 
 
 @pytest.fixture(scope="session")
