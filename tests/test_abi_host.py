@@ -153,6 +153,26 @@ def test_plan_tcgen05_resources(libw4, fmt, bs):
                 assert p["grid"] == min(nrb, SMS)
 
 
+@pytest.mark.parametrize("fmt,bs", [(w4.W4_FMT_NF4, 64), (w4.W4_FMT_INT4, 128), (w4.W4_FMT_FP4, 32)])
+def test_plan_prefill_batch_tiles(libw4, fmt, bs):
+    """Above 128 rows: tiles of 256 batch rows (one 256-column accumulator, the weights decoded once
+    per 256 rows) where the weight matrix has enough 128-row tiles for the SMs, else tiles of 128."""
+    n, k = DECODE["lm_head"]
+    for m in (129, 200, 256):
+        p = _plan(fmt, m, n, k, bs)
+        assert p["kernel"] == w4.W4_KERNEL_TCGEN05 and p["batch_tile"] == 256 and p["launches"] == 1
+        assert p["cluster"] == 1 and p["grid"] == SMS and p["smem_bytes"] <= 227 * 1024
+        # tensor memory: one accumulator of 256 columns, then 32 columns per A stage
+        assert p["stages"] >= 4 and 256 + 32 * p["stages"] <= 512
+    p = _plan(fmt, 512, n, k, bs)
+    assert p["batch_tile"] == 256 and p["launches"] == 2
+    p = _plan(fmt, 300, n, k, bs)
+    assert p["batch_tile"] == 256 and p["launches"] == 2          # 256 + 44
+    # a short weight matrix keeps 128-row batch tiles (its row tiles alone would leave SMs idle)
+    p = _plan(fmt, 256, *DECODE["q"], bs)
+    assert p["batch_tile"] == 128 and p["launches"] == 2
+
+
 def test_plan_split_choices_on_the_decode_shapes(libw4):
     nf4 = w4.W4_FMT_NF4
     # few row tiles and enough K: split over a cluster sized to cover the SMs

@@ -7,7 +7,8 @@ The weights are quantised on the GPU (bit-exact against the oracle on the sample
 sampled output rows are checked one by one against the oracle at the GEMV tolerance.  At batches
 above 8 the lm_head runs on the tcgen05 kernel with 1187 row tiles over 152 CTAs, so every CTA
 takes 7 or 8 tiles: the sample holds rows of each CTA's 1st ... 8th tile for several CTAs, which
-covers both tensor-memory accumulators, their release phases and the scale slots' reuse.
+covers both tensor-memory accumulators (one at 256 batch columns), their release phases and the
+scale slots' reuse.
 """
 import numpy as np
 import pytest
@@ -69,11 +70,14 @@ def sample_rows(ctas=(0, 1, 37, 75, 76, 150, 151), per_tile=3, seed=0):
     return np.unique(np.asarray(rows, dtype=np.int64))
 
 
-@pytest.mark.parametrize("m", [9, 32, 128])
+@pytest.mark.parametrize("m", [9, 32, 128, 256, 300])
 def test_lm_head_full_size_batches(dev, lm_head, m):
+    """Batches 256 and 300 are prefill-sized: tiles of 256 batch rows on one 256-column accumulator
+    (the weights decoded once per 256 rows), 300 = 256 + a 44-row tile."""
     fmt, bs, packed, sc, code = lm_head
     st, plan = w4.w4_gemv_plan(w4._lib.W4_FMT_NF4 if fmt == "nf4" else w4._lib.W4_FMT_INT4, m, N, K, bs)
     assert st == 0 and plan["kernel"] == w4.W4_KERNEL_TCGEN05 and plan["grid"] == 152 and plan["cluster"] == 1
+    assert plan["batch_tile"] == (256 if m > 128 else 128 if m > 64 else 64 if m > 32 else 32 if m > 16 else 16)
     x = synth.activations(synth.x_seed(28, 0, m), m, K)
     X = torch.from_numpy(x).to(dev)
     y = torch.full((m, N), float("nan"), dtype=torch.float16, device=dev)

@@ -223,6 +223,10 @@ TC_CASES = [
     ("int4", 128, 1536, 1536, 128), ("int4", 96, 130, 8960, 32),
     ("fp4", 16, 256, 1536, 32), ("fp4", 9, 8960, 1536, 32), ("fp4", 32, 1536, 8960, 32), ("fp4", 64, 129, 512, 64),
     ("fp4", 128, 1536, 1536, 32), ("fp4", 130, 257, 1024, 32), ("fp4", 20, 100, 160, 32), ("fp4", 40, 100, 96, 32),
+    # prefill-sized batches on weight matrices with enough row tiles: 256-row batch tiles on one
+    # 256-column accumulator (ragged rows, a ragged batch, several tiles per CTA)
+    ("nf4", 256, 20000, 1536, 64), ("int4", 200, 19700, 768, 128), ("fp4", 300, 19500, 512, 32),
+    ("nf4", 129, 19460, 1024, 32),
 ]
 
 

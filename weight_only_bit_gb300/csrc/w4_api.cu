@@ -63,19 +63,49 @@ int check_gemv(int format, const uint8_t* packed, const void* scales, const floa
 // the CUDA cores, whose arithmetic the persistent step kernel shares bit for bit.
 bool tc5_batch(int M) { return M > 8; }
 
-// Largest batch one tensor-core launch takes; larger batches run as tiles of this many rows.
+// Largest batch one tensor-core launch takes with two accumulators; larger batches run as tiles of
+// this many rows, or of twice as many (one 256-column accumulator) where the weight matrix alone
+// has enough 128-row tiles to keep the SMs busy: each tile of weights is then decoded and read once
+// per 256 batch rows instead of once per 128.
 constexpr int kBatchTile = 128;
 
+static bool wide_batch_tiles(int N) {
+  const int nrb = (N + 127) / 128;
+  return 2 * nrb > w4::device_sm_count();
+}
+
+int enqueue_gemv(int format, const uint8_t* packed, const void* scales, const float* codebook, const uint16_t* x,
+                 uint16_t* y, int M, int N, int K, int bs, cudaStream_t stream);
+
+// One batch tile of up to 256 rows on the tcgen05 kernel at 256 columns (above 128 rows), else as
+// tiles of 128.
+static int enqueue_wide_tile(int format, const uint8_t* packed, const void* scales, const float* codebook,
+                             const uint16_t* x, uint16_t* y, int M, int N, int K, int bs, cudaStream_t stream) {
+  if (M > kBatchTile) {
+    cudaError_t e = w4::launch_gemv_tc5(format, packed, scales, codebook, reinterpret_cast<const __half*>(x),
+                                        reinterpret_cast<__half*>(y), M, N, K, bs, true, stream);
+    if (e != cudaErrorNotSupported) return cuda_status(e);
+  }
+  for (int m0 = 0; m0 < M; m0 += kBatchTile) {
+    const int mm = (M - m0) < kBatchTile ? (M - m0) : kBatchTile;
+    const int s = enqueue_gemv(format, packed, scales, codebook, x + (size_t)m0 * K, y + (size_t)m0 * N, mm, N, K,
+                               bs, stream);
+    if (s != W4_OK) return s;
+  }
+  return W4_OK;
+}
+
 // Enqueue one validated GEMV.  Batches above one launch's budget are split into launches over
-// consecutive batch rows (each re-reads the weights): tiles of 128 rows, and within a tile the
-// CUDA-core launches of at most 8 rows where the tensor cores do not serve.
+// consecutive batch rows (each re-reads the weights): tiles of 128 or 256 rows, and within a tile
+// the small-batch launches of at most 8 rows where the tensor cores do not serve.
 int enqueue_gemv(int format, const uint8_t* packed, const void* scales, const float* codebook, const uint16_t* x,
                  uint16_t* y, int M, int N, int K, int bs, cudaStream_t stream) {
   if (M > kBatchTile) {
-    for (int m0 = 0; m0 < M; m0 += kBatchTile) {
-      const int mm = (M - m0) < kBatchTile ? (M - m0) : kBatchTile;
-      const int s = enqueue_gemv(format, packed, scales, codebook, x + (size_t)m0 * K, y + (size_t)m0 * N, mm, N, K,
-                                 bs, stream);
+    const int tile = wide_batch_tiles(N) ? 2 * kBatchTile : kBatchTile;
+    for (int m0 = 0; m0 < M; m0 += tile) {
+      const int mm = (M - m0) < tile ? (M - m0) : tile;
+      const int s = enqueue_wide_tile(format, packed, scales, codebook, x + (size_t)m0 * K, y + (size_t)m0 * N, mm,
+                                      N, K, bs, stream);
       if (s != W4_OK) return s;
     }
     return W4_OK;
@@ -253,7 +283,7 @@ static int check_descs(const w4_gemv_desc* descs, int count) {
   return W4_OK;
 }
 
-// The plan of one batch tile (M <= kBatchTile), validated arguments.
+// The plan of one batch tile (M <= 256), validated arguments.
 static int plan_tile(int format, int M, int N, int K, int blocksize, int sm_count, w4_gemv_plan_t* plan) {
   w4::Tc5Plan tp;
   if (tc5_batch(M) && w4::plan_tc5(M, N, K, blocksize, sm_count, &tp)) {
@@ -274,13 +304,17 @@ int w4_gemv_plan(int format, int M, int N, int K, int blocksize, int sm_count, w
   if (M < 1 || sm_count < 1) return W4_ERR_SHAPE;
   if (M > W4_MAX_BATCH) return W4_ERR_UNSUPPORTED;
   if (M <= kBatchTile) return plan_tile(format, M, N, K, blocksize, sm_count, plan);
-  // full tiles of 128 rows, then the remainder tile; the figures are the full tile's
-  s = plan_tile(format, kBatchTile, N, K, blocksize, sm_count, plan);
+  // full tiles of 128 (or 256) rows, then the remainder tile; the figures are the full tile's
+  w4::Tc5Plan wide;
+  const int tile = 2 * ((N + 127) / 128) > sm_count && w4::plan_tc5(2 * kBatchTile, N, K, blocksize, sm_count, &wide)
+                       ? 2 * kBatchTile
+                       : kBatchTile;
+  s = plan_tile(format, tile, N, K, blocksize, sm_count, plan);
   if (s != W4_OK) return s;
-  plan->launches *= M / kBatchTile;
-  if (M % kBatchTile) {
+  plan->launches *= M / tile;
+  if (M % tile) {
     w4_gemv_plan_t rest;
-    s = plan_tile(format, M % kBatchTile, N, K, blocksize, sm_count, &rest);
+    s = plan_tile(format, M % tile, N, K, blocksize, sm_count, &rest);
     if (s != W4_OK) return s;
     plan->launches += rest.launches;
   }

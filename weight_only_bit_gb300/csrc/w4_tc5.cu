@@ -1,5 +1,5 @@
 // w4_tc5.cu -- fused 4-bit dequant-GEMM on the 5th-generation tensor cores (tcgen05) for batches
-// 9 ... 128 (sm_103a).
+// 9 ... 256 (sm_103a).
 //
 // At these batches every decoded weight feeds 9-128 multiply-adds: the work is a dense
 // contraction and belongs on the tensor cores ("My Triton Kernel Ties bitsandbytes", section "Why
@@ -19,7 +19,9 @@
 //   * B = x: one TMA tensor copy per 64-k stage, NB rows (rows M ... NB - 1 filled with zero by
 //     the copy), 128-byte swizzled, which is the canonical K-major SW128 operand layout;
 //   * D = FP32 accumulators in tensor memory: 128 lanes (weight rows) x NB columns, two of them so
-//     that the epilogue of one tile overlaps the MMAs of the next;
+//     that the epilogue of one tile overlaps the MMAs of the next (NB <= 128), or one of 256
+//     columns for prefill-sized batches (NB = 256: each weight tile is decoded and read once per
+//     256 batch rows; the MMA's N is 256);
 //   * one thread issues four tcgen05.mma.cta_group::1.kind::f16 per stage (K = 16 each) and
 //     commits them to the stage's "empty" barrier; after a tile's last stage, to the
 //     accumulator's "full" barrier;
@@ -202,6 +204,10 @@ __host__ __device__ inline T5Layout t5_layout(int NB, int NP, int NS) {
 
 template <int NB>
 __host__ __device__ constexpr int t5_tmem_cols() { return NB < 32 ? 32 : NB; }
+// Accumulators in tensor memory: two (the epilogue of one tile overlaps the MMAs of the next) up
+// to 128 batch columns; one of 256 columns (the whole accumulator half of tensor memory) at 256.
+template <int NB>
+__host__ __device__ constexpr int t5_nacc() { return NB <= 128 ? 2 : 1; }
 
 // Bounded wait on an mbarrier phase for the pipeline roles.
 __device__ __forceinline__ bool t5_wait(uint64_t* bar, uint32_t parity, uint32_t site) {
@@ -354,9 +360,10 @@ __global__ void __launch_bounds__(kT5Threads, 1) w4_tc5_kernel(const __grid_cons
       constexpr uint32_t idesc = t5_idesc<NB>();
       T5Ring ss{0, 0};
       int tile = 0;
+      constexpr int NACC = t5_nacc<NB>();
       for (int rb = tile0; rb < nrb && ok; rb += tstep, ++tile) {
-        const int b = tile & 1;
-        if (tile >= 2) ok = t5_wait(&accempty[b], ((tile >> 1) - 1) & 1, 0x313);
+        const int b = tile % NACC;
+        if (tile >= NACC) ok = t5_wait(&accempty[b], ((tile / NACC) - 1) & 1, 0x313);
         t5_fence_after();
         const uint32_t d = tmem + (uint32_t)(b * kCols);
         for (int c = c0; c < c1 && ok; ++c) {
@@ -495,9 +502,10 @@ __global__ void __launch_bounds__(kT5Threads, 1) w4_tc5_kernel(const __grid_cons
     // ================================================================ epilogue
     const int g = warp & 3;                          // tensor memory lanes 32g ... 32g + 31
     int tile = 0;
+    constexpr int NACC = t5_nacc<NB>();
     for (int rb = tile0; rb < nrb && ok; rb += tstep, ++tile) {
-      const int b = tile & 1;
-      ok = t5_wait(&accfull[b], (tile >> 1) & 1, 0x318);
+      const int b = tile % NACC;
+      ok = t5_wait(&accfull[b], (tile / NACC) & 1, 0x318);
       if (!ok) break;
       t5_fence_after();
       const uint32_t taddr = tmem + (uint32_t)(b * kCols) + ((uint32_t)(g * 32) << 16);
@@ -566,12 +574,13 @@ __global__ void __launch_bounds__(kT5Threads, 1) w4_tc5_kernel(const __grid_cons
 // kernel does not take.
 bool plan_tc5(int M, int N, int K, int bs, int sms, Tc5Plan* o) {
   // block sizes 32 ... 256 (each thread's 16-k slice lies in one block); K whole 64-k stages
-  if (M < 1 || M > 128 || N < 1 || K < kT5Kc || K % kT5Kc != 0 || bs < 32 || sms < 1) return false;
-  const int NB = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
-  // rings: 4 packed slots (64 KB of weights in flight per SM) and up to 8 stages (the A stages fill
-  // the rest of tensor memory), as many as fit in 227 KB with the 1 KB alignment slack
-  constexpr int NP = 4;
-  static_assert(NP <= kT5Sw, "one scale warp per packed slot");
+  if (M < 1 || M > 2 * kT5Rows || N < 1 || K < kT5Kc || K % kT5Kc != 0 || bs < 32 || sms < 1) return false;
+  const int NB = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  // rings: 4 packed slots (64 KB of weights in flight per SM; 3 at 256 batch columns, whose x
+  // stages are 32 KB) and up to 8 stages (the A stages fill the rest of tensor memory), as many as
+  // fit in 227 KB with the 1 KB alignment slack
+  const int NP = NB == 256 ? 3 : 4;
+  static_assert(4 <= kT5Sw, "one scale warp per packed slot");
   int NS = 0;
   for (int ns = kT5MaxStages; ns >= 4 && NS == 0; --ns) {
     if (t5_layout(NB, NP, ns).total + 1024 <= 227 * 1024) NS = ns;
@@ -664,6 +673,9 @@ cudaError_t launch_gemv_tc5(int format, const uint8_t* packed, const void* scale
     case 2032: return launch_tc5_nb<2, 32>(p, pl, pdl, stream);
     case 2064: return launch_tc5_nb<2, 64>(p, pl, pdl, stream);
     case 2128: return launch_tc5_nb<2, 128>(p, pl, pdl, stream);
+    case 256: return launch_tc5_nb<0, 256>(p, pl, pdl, stream);
+    case 1256: return launch_tc5_nb<1, 256>(p, pl, pdl, stream);
+    case 2256: return launch_tc5_nb<2, 256>(p, pl, pdl, stream);
     default: return cudaErrorNotSupported;
   }
 }
