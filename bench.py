@@ -500,6 +500,13 @@ def run_ours(args):
                 sh, _ = per_shape(fmt, dev, torch, hbm, M=M, tflops_peak=tfp, only={"gate", "down", "q"})
                 c4[f"{fmt}_b{M}"] = sh
         extra["c4_small_batches"] = c4
+        # prefill-sized batches on the lm_head: 256-row batch tiles (one pass over the weights per
+        # 256 rows)
+        pre = {}
+        for M in (256, 512):
+            sh, _ = per_shape("nf4", dev, torch, hbm, M=M, tflops_peak=tfp, only={"lm_head"})
+            pre[f"nf4_b{M}"] = sh["lm_head"]
+        extra["prefill_lm_head"] = pre
         # read-only streaming ceiling: a library reduction reading a 2 GiB buffer once per pass
         buf = torch.ones(1 << 29, dtype=torch.float32, device=dev)
         with torch.cuda.stream(stream):
