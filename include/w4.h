@@ -234,6 +234,15 @@ int w4_step_create(const w4_gemv_desc* descs, int count, void* workspace, w4_ste
 int w4_step_launch(w4_step* step, w4_stream_t stream);
 int w4_step_destroy(w4_step* step);
 
+/* w4_step_run_host -- one step with host buffers, all on `stream` and asynchronous: copies x_bytes
+ * from x_host to the step's device input x_dev, launches the step, copies y_bytes from the step's
+ * device output y_dev to y_host.  Host buffers should be pinned (page-locked) for the copies to
+ * overlap; the caller synchronises `stream` before reading y_host.  x_bytes or y_bytes 0 skips that
+ * copy.  Errors: W4_ERR_NULL (step, or a buffer of a non-empty copy), W4_ERR_SHAPE (negative
+ * size), W4_ERR_CUDA. */
+int w4_step_run_host(w4_step* step, const void* x_host, void* x_dev, int64_t x_bytes, void* y_host,
+                     const void* y_dev, int64_t y_bytes, w4_stream_t stream);
+
 /* ---------------------------------------------------------------------------------------
  * w4_gemv_levels_noalloc -- runs the descriptors as ONE persistent launch on `stream`, like
  * w4_step_create + w4_step_launch, without any device memory from the caller beyond its inputs

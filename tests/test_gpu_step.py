@@ -74,6 +74,31 @@ def test_full_step_graph(dev, fmt, levels):
     step.close()
 
 
+def test_step_with_host_buffers(dev):
+    """w4_step_run_host: x copied in from pinned host memory, the step, y copied out; the host y
+    equals the device y of a plain launch bit for bit, and a changed host x reaches the kernels."""
+    from weight_only_bit_gb300.step import DecodeStep
+    step = DecodeStep("nf4", batch=1, device=str(dev), layers=1, lm_head=False).build().capture()
+    stream = torch.cuda.Stream(dev)
+    w4.check(step.launch(stream))
+    torch.cuda.synchronize()
+    ref = step.y.cpu().clone()
+    x_pin = torch.from_numpy(step.x_host.copy()).pin_memory()
+    y_pin = torch.full((step.y_elems,), float("nan"), dtype=torch.float16).pin_memory()
+    step.x.zero_()
+    w4.check(step.run_host(x_pin, y_pin, stream))
+    stream.synchronize()
+    assert w4.w4_device_check(stream) == 0
+    assert torch.equal(y_pin.view(torch.int16), ref.view(torch.int16))
+    x_pin.mul_(2)                                  # exact in FP16: every y doubles exactly
+    w4.check(step.run_host(x_pin, y_pin, stream))
+    stream.synchronize()
+    assert torch.equal(y_pin.view(torch.int16), (ref.float() * 2).half().view(torch.int16))
+    assert w4.w4_step_run_host(None, x_pin, step.x, 2, y_pin, step.y, 2) == w4._lib.W4_ERR_NULL
+    assert w4.w4_step_run_host(step.step, x_pin, step.x, -1, y_pin, step.y, 2) == w4._lib.W4_ERR_SHAPE
+    step.close()
+
+
 @pytest.mark.parametrize("fmt,batch", [("int4", 1), ("nf4", 3), ("nf4", 8), ("int4", 8), ("nf4", 32), ("fp4", 2),
                                        ("fp4", 8), ("fp4", 32)])
 def test_reduced_steps(dev, fmt, batch):

@@ -19,7 +19,7 @@ __all__ = [
     "w4_step_launch",
     "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check", "w4_launch_count",
     "w4_inject_timeout_once", "w4_gemv_levels_noalloc", "w4_gemv_plan",
-    "w4_quantize_fp4", "w4_dequantize_fp4", "w4_gemv_fp4",
+    "w4_quantize_fp4", "w4_dequantize_fp4", "w4_gemv_fp4", "w4_step_run_host",
     "check", "W4Error", "GemvDesc", "GemvPlan", "W4_FMT_NF4", "W4_FMT_INT4", "W4_FMT_FP4", "W4_MAX_BATCH",
     "W4_MAX_K",
     "W4_KERNEL_SMALL_BATCH", "W4_KERNEL_TCGEN05",
@@ -124,6 +124,13 @@ def w4_step_create(descs, workspace):
 
 def w4_step_launch(step, stream=None):
     return lib().w4_step_launch(step, _stream(stream))
+
+
+def w4_step_run_host(step, x_host, x_dev, x_bytes, y_host, y_dev, y_bytes, stream=None):
+    """x_host / y_host: pinned host tensors (or raw addresses); x_dev / y_dev: the step's device
+    input and output buffers."""
+    return lib().w4_step_run_host(step, _ptr(x_host), _ptr(x_dev), x_bytes, _ptr(y_host), _ptr(y_dev), y_bytes,
+                                  _stream(stream))
 
 
 def w4_step_destroy(step):

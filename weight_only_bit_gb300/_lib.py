@@ -36,7 +36,7 @@ SYMBOLS = (
     "w4_dequantize_int4", "w4_gemv_nf4", "w4_gemv_int4", "w4_gemv_sequence", "w4_step_workspace_bytes", "w4_step_create",
     "w4_step_launch", "w4_step_destroy", "w4_status_str", "w4_last_cuda_error", "w4_device_check",
     "w4_launch_count", "w4_inject_timeout_once", "w4_gemv_levels_noalloc", "w4_gemv_plan",
-    "w4_quantize_fp4", "w4_dequantize_fp4", "w4_gemv_fp4",
+    "w4_quantize_fp4", "w4_dequantize_fp4", "w4_gemv_fp4", "w4_step_run_host",
 )
 
 
@@ -99,6 +99,7 @@ def _declare(L):
         "w4_step_create": (I, [ctypes.POINTER(GemvDesc), I, P, ctypes.POINTER(P)]),
         "w4_step_launch": (I, [P, P]),
         "w4_step_destroy": (I, [P]),
+        "w4_step_run_host": (I, [P, P, P, ctypes.c_int64, P, P, ctypes.c_int64, P]),
         "w4_status_str": (ctypes.c_char_p, [I]),
         "w4_last_cuda_error": (I, []),
         "w4_device_check": (I, [P]),

@@ -454,6 +454,22 @@ int w4_step_launch(w4_step* step, w4_stream_t stream) {
   return cuda_status(e);
 }
 
+int w4_step_run_host(w4_step* step, const void* x_host, void* x_dev, int64_t x_bytes, void* y_host,
+                     const void* y_dev, int64_t y_bytes, w4_stream_t stream) {
+  if (!step || !step->exec) return W4_ERR_NULL;
+  if (x_bytes < 0 || y_bytes < 0) return W4_ERR_SHAPE;
+  if ((x_bytes > 0 && (!x_host || !x_dev)) || (y_bytes > 0 && (!y_host || !y_dev))) return W4_ERR_NULL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (x_bytes > 0) e = cudaMemcpyAsync(x_dev, x_host, (size_t)x_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = cudaGraphLaunch(step->exec, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  w4::g_launches.fetch_add(step->kernels);
+  if (y_bytes > 0) e = cudaMemcpyAsync(y_host, y_dev, (size_t)y_bytes, cudaMemcpyDeviceToHost, s);
+  return cuda_status(e);
+}
+
 int w4_step_destroy(w4_step* step) {
   if (!step) return W4_ERR_NULL;
   if (step->exec) cudaGraphExecDestroy(step->exec);

@@ -121,6 +121,12 @@ class DecodeStep:
     def launch(self, stream=None):
         return w4.w4_step_launch(self.step, stream)
 
+    def run_host(self, x_host, y_host, stream=None):
+        """One step from and to host buffers (pinned tensors of the x and y arenas' sizes) through
+        the library's w4_step_run_host."""
+        return w4.w4_step_run_host(self.step, x_host, self.x, self.x_elems * 2, y_host, self.y, self.y_elems * 2,
+                                   stream)
+
     def enqueue_eager(self, stream=None):
         """One launch per GEMV, back to back (the same results, without the persistent step)."""
         return w4.w4_gemv_sequence(self.descriptors(), stream)
