@@ -71,7 +71,7 @@ typedef enum {
 typedef enum { W4_FMT_NF4 = 0, W4_FMT_INT4 = 1, W4_FMT_FP4 = 2 } w4_format;
 
 /* Limits of this build. */
-#define W4_MAX_BATCH 4096       /* M; above 128, batch tiles of 128 rows (prefill-sized)       */
+#define W4_MAX_BATCH 4096       /* M; above 128, batch tiles of 128 or 256 rows (prefill-sized) */
 #define W4_MAX_K 10240          /* K; sizes the batch 1 ... 8 kernel's partial-sum buffers     */
 
 /* ---------------------------------------------------------------------------------------
@@ -141,8 +141,9 @@ int w4_dequantize_fp4(const uint8_t* packed, const uint16_t* scale, float* W_out
  * table into warp-level mma.sync FP16 x FP16 -> FP32 products, block scales applied to the FP32
  * partial sums); batches 9 ... 128 on the 5th-generation tensor cores (tcgen05) when K is a
  * multiple of 64, else in 8-row launches of the small-batch kernel.  Larger batches
- * (prefill-sized, up to W4_MAX_BATCH) run as tiles of 128 batch rows, each tile one pass over
- * the weights.
+ * (prefill-sized, up to W4_MAX_BATCH) run as tiles of batch rows, each tile one pass over the
+ * weights: 256 rows (one 256-column accumulator) where the matrix has at least half as many
+ * 128-row tiles as the GPU has SMs, else 128.
  * Sizes: 1 <= M <= W4_MAX_BATCH, N >= 1, 32 <= K <= W4_MAX_K, K % blocksize == 0,
  * blocksize a power of two in [32, 256].  packed, scales, x 16-byte aligned; y 2-byte aligned.
  * Agreement with the float64 definition: relative L2 error <= 1e-3 and
