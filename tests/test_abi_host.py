@@ -228,3 +228,12 @@ def test_plan_prefill_batches_run_as_128_row_tiles(libw4):
     assert _plan(nf4, 130, *DECODE["q"], 64)["launches"] == 2
     # K not a multiple of 64: CUDA-core launches of 8 rows throughout
     assert _plan(nf4, 300, 100, 96, 32)["launches"] == 38
+
+
+def test_step_run_host_validates_on_the_host(libw4):
+    """w4_step_run_host rejects a missing step, missing buffers of a non-empty copy and negative
+    sizes before any CUDA call (no GPU needed)."""
+    L = libw4
+    assert L.w4_step_run_host(None, None, None, 0, None, None, 0, None) == w4.W4_ERR_NULL
+    fake = ctypes.c_void_p(0)
+    assert L.w4_step_run_host(fake, None, None, 0, None, None, 0, None) == w4.W4_ERR_NULL   # no graph
