@@ -272,6 +272,22 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------------- GPU arm
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time per step (replicas: every rank times the same workload)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the bytes every rank moved in one step over the slowest rank's time."""
+    return bytes_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
 def time_graph(step, stream, steps, warmup, torch):
     for _ in range(warmup):
         step.launch(stream)
@@ -410,11 +426,8 @@ def run_ours(args):
         dist.barrier()
     w4.check(w4.w4_device_check(stream), "timed region")
     ms = e0.elapsed_time(e1) / args.steps
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = nbytes * world / (ms_max * 1e-3) / 1e9
+    ms_max = max_over_ranks(ms, world, dev)
+    value = job_gbs(nbytes, world, ms_max)
 
     # distribution of single steps (each bracketed by its own events, back to back, after the
     # timed region): p10 / median / p90
