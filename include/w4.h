@@ -280,7 +280,7 @@ int w4_device_check(w4_stream_t stream);
 /* Kernel launches the library has issued in this process (for launch accounting). */
 long long w4_launch_count(void);
 
-/* Test hook for the timeout path.  The next GEMV launch in this process (CUDA-core or tcgen05
+/* Test hook for the timeout path.  The next GEMV launch in this process (small-batch or tcgen05
  * kernel, whichever the call dispatches to) has its weight producer issue no copies, so the bounded
  * waits (one second each) of the roles that depend on those copies run out; the kernel records the
  * failure, waits (bounded) for whatever copies and MMAs it did issue, frees its tensor memory and

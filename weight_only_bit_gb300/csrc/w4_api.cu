@@ -60,7 +60,7 @@ int check_gemv(int format, const uint8_t* packed, const void* scales, const floa
 }
 
 // Batches above 8 go to the tcgen05 kernel (where it takes the shape); batches up to 8 stay on
-// the CUDA cores, whose arithmetic the persistent step kernel shares bit for bit.
+// the small-batch kernel, the same kernel (and arithmetic, bit for bit) as the persistent step.
 bool tc5_batch(int M) { return M > 8; }
 
 // Largest batch one tensor-core launch takes with two accumulators; larger batches run as tiles of
@@ -113,10 +113,10 @@ int enqueue_gemv(int format, const uint8_t* packed, const void* scales, const fl
   const __half* xh = reinterpret_cast<const __half*>(x);
   __half* yh = reinterpret_cast<__half*>(y);
   // batches above 8: the 5th-generation tensor cores (tcgen05; a batch below 16 is padded to 16
-  // MMA columns at no extra MMA cost).  Batches up to 8 stay on the CUDA cores, whose arithmetic
-  // the persistent step kernel shares bit for bit.  Both tensor-core kernels need K to be a
-  // multiple of 64; the mma.sync one (batch >= 32) also serves if the TMA descriptors cannot be
-  // made.  Everything else runs on the CUDA cores.
+  // MMA columns at no extra MMA cost).  Batches up to 8 stay on the small-batch kernel, whose
+  // arithmetic the persistent step kernel shares bit for bit.  Both batch >= 9 kernels need K to
+  // be a multiple of 64; the mma.sync one (batch >= 32) also serves if the TMA descriptors cannot
+  // be made.  Everything else runs as small-batch launches of at most 8 rows.
   if (tc5_batch(M)) {
     cudaError_t e = w4::launch_gemv_tc5(format, packed, scales, codebook, xh, yh, M, N, K, bs, true, stream);
     if (e != cudaErrorNotSupported) return cuda_status(e);
@@ -348,7 +348,7 @@ int64_t w4_step_workspace_bytes(int count) {
   return ((int64_t)ws_counter_bytes(count) + 128 + (int64_t)w4::step_tables_bytes(count) + 255) / 256 * 256;
 }
 
-// True when the step can run as one persistent CUDA-core launch.
+// True when the step can run as one persistent launch of the small-batch kernel.
 static bool step_is_persistent(const w4_gemv_desc* descs, int count) {
   if (count > w4::kStepMaxGemvs) return false;
   for (int i = 0; i < count; ++i) {
@@ -498,7 +498,7 @@ int w4_last_cuda_error(void) { return t_last_cuda_error; }
 int w4_device_check(w4_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_status(e);
-  // every translation unit's copy of the error word: the CUDA-core and the tensor-core kernels
+  // every translation unit's copy of the error word: the small-batch and the tensor-core kernels
   const unsigned int v = w4::read_clear_error_persist() | w4::read_clear_error_tc5();
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e);

@@ -1,4 +1,4 @@
-// w4_mma_unit.cuh -- the decode-and-multiply unit of the batch 1 ... 8 kernel: 16 weight rows x 256 k
+// w4_mma_unit.cuh -- the decode-and-multiply unit of the batch 1 ... 8 kernel: 16 weight rows x 128 k
 // of a tile in shared memory, decoded through the byte-pair table into mma.sync.m16n8k16 A fragments
 // (FP16 x FP16 -> FP32) against x, with the block scales applied to FP32 accumulators.
 #pragma once

@@ -16,8 +16,9 @@
 // one CTA per SM, all co-resident.
 //
 // The arithmetic runs on the tensor cores through warp-level mma.sync.m16n8k16 (FP16 x FP16 ->
-// FP32), with the weights as the A operand and x (batch rows 0 ... 7, zero above the batch) as B:
-//   * a warp's unit of work is 16 rows x 256 k of one tile (a "span"): per 64-k block (32-k block
+// FP32), with the weights as the A operand and x (batch rows 0 ... 7; columns at or above the batch
+// are computed from the last batch row and never stored) as B:
+//   * a warp's unit of work is 16 rows x 128 k of one tile (a "span"): per 64-k block (32-k block
 //     when the scale block is 32) lane (g, t) = (lane / 4, lane % 4) reads the 8 (4) consecutive
 //     packed bytes 8t ... 8t + 7 of the rows its MMA rows g and g + 8 stand for (tile rows 2g and
 //     2g + 1 of the row group with 64-k blocks, g and g + 8 with 32-k blocks, the pairing that keeps
@@ -29,11 +30,11 @@
 //   * the MMAs of one scale block start from zero, and the block's scale (FP32 absmax for NF4,
 //     FP16 scale for INT4 and FP4) multiplies the result into the unit's FP32 accumulators;
 //   * each unit leaves one FP32 partial per (batch row, weight row, span) in shared memory, and the
-//     reducer warp sums a row's spans in a fixed order (span 0, 1, 2, ...).  The split of K into
-//     spans depends only on K, so a row gets the same bits whatever the tiling.
+//     reducer warp sums a row's spans in an order that depends only on K (eight interleaved
+//     sequences, then a fixed tree), so a row gets the same bits whatever the tiling.
 // Roles in a CTA:
-//   * producer warp: copies each tile into a shared-memory ring with one 2-D TMA tensor copy per span
-//     (a box of 128 bytes x the tile's rows, 128-byte swizzled: the 16-byte chunk c of tile row r
+//   * producer warp: copies each tile into a shared-memory ring with one 2-D TMA tensor copy per
+//     256-k box (128 bytes x the tile's rows, 128-byte swizzled: the 16-byte chunk c of tile row r
 //     lands at chunk c ^ (r & 7), so the fragment loads of a warp hit distinct banks) and its scales
 //     with one 1-D bulk copy, completion on the stage's mbarrier.  Weights never depend on other
 //     GEMVs, so it runs ahead across level boundaries.  Copies are issued only while the CTA's
@@ -42,8 +43,9 @@
 //     level's completion is published and the next level waits slows that release and its polls.
 //     The consumers open the gate before they wait for a level's first tile, so a tile held back
 //     at a level's end is issued as soon as the level starts;
-//   * 14 consumer warps (16 warps in all, so each thread may hold 128 registers): the units of each tile, round-robin over the warps (continuing across
-//     tiles, so an uneven tile does not always load the same warps);
+//   * 14 consumer warps (16 warps in all, so each thread may hold 128 registers): the units of
+//     each tile, round-robin over the warps (continuing across tiles, so an uneven tile does not
+//     always load the same warps);
 //   * reducer warp: sums each row's partials, writes y, and after the CTA's last tile of a level
 //     publishes completion with one release, before it reads any table entry of the next tile
 //     (whether a tile ends the CTA's part of a level is known from the cursor alone).
