@@ -13,6 +13,7 @@
 namespace w4 {
 
 constexpr int kLutBytes = 256 * 32 * 4;   // byte-pair table, one copy per lane
+constexpr int kLutWideBytes = 256 * 64 * 4;   // the same at 256-byte entry stride (build_lut, wide)
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
@@ -50,13 +51,17 @@ __device__ __forceinline__ float nibble_value(int fmt, const float* __restrict__
   return (q & 8) ? -v : v;
 }
 
+// wide = false: entry b of lane l at word 32 b + l (32 KB).  wide = true: at word 64 b + l (64 KB),
+// so that entry b of lane l sits at byte 256 b + 4 l, an offset one byte permute forms from the
+// packed byte and the lane; words 64 b + 32 ... 64 b + 63 are left free (256 gaps of 128 bytes).
 __device__ __forceinline__ void build_lut(uint32_t* lut, int fmt, const float* __restrict__ codebook, int t,
-                                          int nthreads) {
+                                          int nthreads, bool wide = false) {
+  const int sh = wide ? 6 : 5;
   for (int i = t; i < 256 * 32; i += nthreads) {
     const int b = i >> 5;
     const __half lo = __float2half_rn(nibble_value(fmt, codebook, b >> 4));
     const __half hi = __float2half_rn(nibble_value(fmt, codebook, b & 15));
-    lut[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+    lut[(b << sh) + (i & 31)] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
   }
 }
 

@@ -37,6 +37,11 @@ __device__ __forceinline__ uint2 lds_ring64(uint32_t a) {
   asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
 }
+// Shared-memory store that only lanes with `pred` perform (a predicated store, no branch).
+__device__ __forceinline__ void sts_f32_if(uint32_t a, float v, bool pred) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p st.shared.f32 [%0], %1;\n}"
+               ::"r"(a), "f"(v), "r"((int)pred) : "memory");
+}
 __device__ __forceinline__ float lds_scale32(uint32_t a) { return __uint_as_float(lds_ring32(a)); }
 __device__ __forceinline__ float lds_scale16(uint32_t a) {
   unsigned short v;
@@ -45,12 +50,39 @@ __device__ __forceinline__ float lds_scale16(uint32_t a) {
 }
 
 // Decoded pair (element 2j in the low half) of packed byte b (0 ... 3) of word w, from this lane's
-// copy of the byte-pair table (lut_lane: shared address of the lane's entry 0).
-__device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lane, uint32_t w, int b) {
+// copy of the byte-pair table.  32 KB table: lut = shared address of the lane's entry 0.  64 KB
+// table (WIDE): lut = the table's shared address (the same in every lane) and lane4 = 4 * lane; one
+// byte permute forms the entry's offset 256 * byte + lane4.
+template <bool WIDE>
+__device__ __forceinline__ uint32_t lut_pair(uint32_t lut, uint32_t lane4, uint32_t w, int b) {
+  if (WIDE) {
+    uint32_t off;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(off) : "r"(w), "r"(lane4), "r"(0x5504 | (b << 4)));
+    return lds_table(lut + off);
+  }
   uint32_t byte;
   asm("prmt.b32 %0, %1, 0, %2;" : "=r"(byte) : "r"(w), "r"(0x4440 + b));
-  return lds_table(lut_lane + (byte << 7));
+  return lds_table(lut + (byte << 7));
 }
+
+// Where a tile's span partials live.  Dense: output o's partial of span c at float o * cp + c of
+// the buffer.  Gaps (the 64 KB table's 128-byte gaps, 32 floats each): output o owns hpo
+// consecutive gaps from gap o * hpo, span c in gap c / 32 at word (c + 4 (o & 7)) mod 32 (the
+// rotation puts eight consecutive outputs' runs of four spans in distinct banks); base = the
+// buffer's first gap, gaps 256 bytes apart.  at(o, c) with c a multiple of 4 starts four
+// consecutive spans (16-byte aligned).
+struct PartDense {
+  const float* base;
+  int cp;
+  __device__ __forceinline__ const float* at(int o, int c) const { return base + o * cp + c; }
+};
+struct PartGaps {
+  const uint8_t* base;
+  int hpo;
+  __device__ __forceinline__ const float* at(int o, int c) const {
+    return reinterpret_cast<const float*>(base + ((o * hpo + (c >> 5)) << 8)) + (((c & 31) + 4 * (o & 7)) & 31);
+  }
+};
 
 // Sum of one output's span partials rr[0 .. C) in an order that depends only on C: eight
 // interleaved sequences s_i = rr[i] + rr[i + 8] + ... (each from 0, in index order), then
@@ -59,8 +91,8 @@ __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lane, uint32_t w, int 
 // and the group combines them with shuffles along the same tree (IEEE addition is commutative,
 // so both lanes of a pair get the same bits).  Every lane of the warp must call it; the result
 // is the same for every Q.
-template <int Q>
-__device__ __forceinline__ float sum_spans(const float* rr, int C, int sub) {
+template <int Q, class Part>
+__device__ __forceinline__ float sum_spans(const Part& P, int o, int C, int sub) {
   constexpr int NK = 8 / Q;
   float s[NK];
 #pragma unroll
@@ -69,7 +101,7 @@ __device__ __forceinline__ float sum_spans(const float* rr, int C, int sub) {
 #pragma unroll
     for (int k = 0; k < NK; ++k) {
       const int i = j + sub + Q * k;
-      if (i < C) s[k] += rr[i];
+      if (i < C) s[k] += *P.at(o, i);
     }
   }
   if (Q >= 2) {
@@ -86,13 +118,12 @@ __device__ __forceinline__ float sum_spans(const float* rr, int C, int sub) {
   return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
-// The same sum (one lane per output) for R outputs at once, rr[r] the partials of output r (16-byte
-// aligned; the eight floats of each group of eight spans may be read past C): every load of a
-// group of eight spans is issued before the first add, as two 16-byte loads per output, so a pass
-// costs one shared-memory round trip per eight spans for all R outputs (the queue is long while
-// the units decode).
-template <int R>
-__device__ __forceinline__ void sum_spans_batch(float (&out)[R], const float* const (&rr)[R], int C) {
+// The same sum (one lane per output) for R outputs o[r] at once (the eight floats of each group of
+// eight spans may be read past C): every load of a group of eight spans is issued before the first
+// add, as two 16-byte loads per output, so a pass costs one shared-memory round trip per eight
+// spans for all R outputs (the queue is long while the units decode).
+template <int R, class Part>
+__device__ __forceinline__ void sum_spans_batch(float (&out)[R], const Part& P, const int (&o)[R], int C) {
   float s[R][8];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -103,8 +134,8 @@ __device__ __forceinline__ void sum_spans_batch(float (&out)[R], const float* co
     float4 v[R][2];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      v[r][0] = *reinterpret_cast<const float4*>(rr[r] + j);
-      v[r][1] = *reinterpret_cast<const float4*>(rr[r] + j + 4);
+      v[r][0] = *reinterpret_cast<const float4*>(P.at(o[r], j));
+      v[r][1] = *reinterpret_cast<const float4*>(P.at(o[r], j + 4));
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -157,31 +188,12 @@ __device__ __forceinline__ void span_scales(float (&sk)[kSpanK / KB], uint32_t a
   for (int j = 0; j < NKB; ++j) sk[j] = v[j / (NKB / NSC)];
 }
 
-// One unit: 16 weight rows x one span (128 k) of a tile.  a0, a1: shared addresses of the span's
-// row of MMA row g and of MMA row g + 8 (128 bytes each); off0[j], off1[j]: this lane's byte offset
-// of k block j in those swizzled rows; s0a, s1a: their scale rows (at the span's first scale); v0 /
-// v1 false for rows beyond the tile (their scales are zeroed); xg: this lane's x elements of the
-// span (lanes whose batch row g is at or above the batch read the last batch row instead: their
-// MMA columns are never stored).  NSC > 0: the span is full and its NSC scales per row are one aligned vector (K a
-// multiple of 128); NSC == 0: the general case, nkb k blocks present, scale index of block j =
-// sidx0 + (j >> sshift) relative to s0a / s1a.
-// KB = 64: per 64-k block, 8 packed bytes per lane per row and 4 MMAs; KB = 32: 4 bytes, 2 MMAs.
-// acc[0], acc[1]: MMA row g, batch rows 2t, 2t + 1; acc[2], acc[3]: MMA row g + 8.
-template <int KB, bool SC32, int NSC>
-__device__ __forceinline__ void mma_unit(float (&acc)[4], uint32_t a0, uint32_t a1, const uint32_t (&off0)[kSpanK / KB],
-                                         const uint32_t (&off1)[kSpanK / KB], uint32_t s0a, uint32_t s1a,
-                                         bool v0, bool v1, const uint8_t* xg, int sidx0, int sshift, int nkb,
-                                         uint32_t lut_lane, int lane) {
-  constexpr int NKB = kSpanK / KB;     // k blocks per full span
-  constexpr int RUN = KB / 8;          // packed bytes per lane per row per k block
-  constexpr int NMMA = KB / 16;        // MMAs per k block
-  constexpr bool FULL = NSC > 0;
-  constexpr int ES = SC32 ? 4 : 2;
-  const int t = lane & 3;
-  // x of this lane's batch row: KB/4 halves (KB/2 bytes) per k block
-  uint32_t xr[NKB][KB / 8];
+// x of one span for this lane: KB / 4 halves per k block (16-byte loads from xg; blocks at or past
+// nkb are zero unless the span is full).
+template <int KB, bool FULL>
+__device__ __forceinline__ void load_span_x(uint32_t (&xr)[kSpanK / KB][KB / 8], const uint8_t* xg, int nkb) {
 #pragma unroll
-  for (int j = 0; j < NKB; ++j) {
+  for (int j = 0; j < kSpanK / KB; ++j) {
 #pragma unroll
     for (int q = 0; q < KB / 32; ++q) {
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -189,18 +201,50 @@ __device__ __forceinline__ void mma_unit(float (&acc)[4], uint32_t a0, uint32_t 
       xr[j][4 * q + 0] = v.x; xr[j][4 * q + 1] = v.y; xr[j][4 * q + 2] = v.z; xr[j][4 * q + 3] = v.w;
     }
   }
+}
+
+// d = A * B (the accumulator input is zero).
+__device__ __forceinline__ void mma16816_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// One unit: 16 weight rows x one span (128 k) of a tile.  b0, b1: shared address of the span's row
+// of MMA row g and of MMA row g + 8 (row starts, multiples of 128) plus 64 when the span is the
+// second half of its box; the lane's bytes of k block j sit at b0 ^ off0[j] and b1 ^ off1[j]
+// (off < 128 holds the lane's byte offset and the row's swizzle).  s0a, s1a: the two rows' scale
+// rows (at the span's first scale).  xr: this lane's x of the span (load_span_x; lanes whose batch
+// row g is at or above the batch hold the last batch row: their MMA columns are never stored).
+// NSC > 0: the span is full and its NSC scales per row are one aligned vector (K a multiple of
+// 128); NSC == 0: the general case, nkb k blocks present, scale index of block j = sidx0 +
+// (j >> sshift) relative to s0a / s1a.  MMA rows past the tile hold whatever the ring holds there;
+// rows are independent in the MMA and those results are never stored.
+// KB = 64: per 64-k block, 8 packed bytes per lane per row and 4 MMAs; KB = 32: 4 bytes, 2 MMAs.
+// acc[0], acc[1]: MMA row g, batch rows 2t, 2t + 1; acc[2], acc[3]: MMA row g + 8.
+template <int KB, bool SC32, int NSC, bool WIDE>
+__device__ __forceinline__ void mma_unit(float (&acc)[4], uint32_t b0, uint32_t b1, const uint32_t (&off0)[kSpanK / KB],
+                                         const uint32_t (&off1)[kSpanK / KB], uint32_t s0a, uint32_t s1a,
+                                         const uint32_t (&xr)[kSpanK / KB][KB / 8], int sidx0, int sshift, int nkb,
+                                         uint32_t lut, int lane) {
+  constexpr int NKB = kSpanK / KB;     // k blocks per full span
+  constexpr int RUN = KB / 8;          // packed bytes per lane per row per k block
+  constexpr int NMMA = KB / 16;        // MMAs per k block
+  constexpr bool FULL = NSC > 0;
+  constexpr int ES = SC32 ? 4 : 2;
+  const int t = lane & 3;
   // packed bytes of both rows, per k block
   uint32_t w0[NKB][RUN / 4], w1[NKB][RUN / 4];
 #pragma unroll
   for (int j = 0; j < NKB; ++j) {
     if (FULL || j < nkb) {
       if (RUN == 8) {
-        const uint2 p = lds_ring64(a0 + off0[j]), q = lds_ring64(a1 + off1[j]);
+        const uint2 p = lds_ring64(b0 ^ off0[j]), q = lds_ring64(b1 ^ off1[j]);
         w0[j][0] = p.x; w0[j][RUN / 4 - 1] = p.y;
         w1[j][0] = q.x; w1[j][RUN / 4 - 1] = q.y;
       } else {
-        w0[j][0] = lds_ring32(a0 + off0[j]);
-        w1[j][0] = lds_ring32(a1 + off1[j]);
+        w0[j][0] = lds_ring32(b0 ^ off0[j]);
+        w1[j][0] = lds_ring32(b1 ^ off1[j]);
       }
     } else {
 #pragma unroll
@@ -236,21 +280,18 @@ __device__ __forceinline__ void mma_unit(float (&acc)[4], uint32_t a0, uint32_t 
   }
 #pragma unroll
   for (int j = 0; j < NKB; ++j) {
-    if (!v0) sk0[j] = 0.0f;
-    if (!v1) sk1[j] = 0.0f;
-  }
-#pragma unroll
-  for (int j = 0; j < NKB; ++j) {
     if (FULL || j < nkb) {
-      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float d[4];
 #pragma unroll
       for (int s = 0; s < NMMA; ++s) {
         // slot t: packed byte 2s of the lane's run (k 4s, 4s + 1); slot t + 4: byte 2s + 1
         const uint32_t ww0 = w0[j][(2 * s) >> 2], ww1 = w1[j][(2 * s) >> 2];
         const int b = (2 * s) & 3;
-        const uint32_t a[4] = {lut_pair(lut_lane, ww0, b), lut_pair(lut_lane, ww1, b), lut_pair(lut_lane, ww0, b + 1),
-                               lut_pair(lut_lane, ww1, b + 1)};
-        mma16816(d, a, xr[j][2 * s], xr[j][2 * s + 1]);
+        const uint32_t l4 = (uint32_t)lane * 4u;
+        const uint32_t a[4] = {lut_pair<WIDE>(lut, l4, ww0, b), lut_pair<WIDE>(lut, l4, ww1, b),
+                               lut_pair<WIDE>(lut, l4, ww0, b + 1), lut_pair<WIDE>(lut, l4, ww1, b + 1)};
+        if (s == 0) mma16816_first(d, a, xr[j][2 * s], xr[j][2 * s + 1]);
+        else mma16816(d, a, xr[j][2 * s], xr[j][2 * s + 1]);
       }
       acc[0] = fmaf(sk0[j], d[0], acc[0]);
       acc[1] = fmaf(sk0[j], d[1], acc[1]);

@@ -146,18 +146,26 @@ struct PLayout {
   int lut, w, s, red, bar, total;
 };
 
-__host__ __device__ inline PLayout playout(int stages, int stage_w, int stage_s, int red_floats) {
+// The 64 KB table's gaps (entry b's bytes 128 ... 255) hold the two partial-sum buffers at batch 1:
+// gaps 0 ... 127 the first, 128 ... 255 the second.
+constexpr int kGapOffset = 128;
+constexpr int kGapsPerBuf = 128;
+constexpr int kGapBufBytes = kGapsPerBuf * 256;
+__host__ __device__ constexpr int gaps_per_output(int nspan) { return (nspan + 31) >> 5; }
+
+// wide: the 64 KB table, the partial sums in its gaps (red_floats unused).
+__host__ __device__ inline PLayout playout(int stages, int stage_w, int stage_s, int red_floats, bool wide) {
   PLayout L;
   int off = 0;
   L.lut = off;
-  off += kLutBytes;           // 32 KB: the ring starts 1 KB aligned
+  off += wide ? kLutWideBytes : kLutBytes;   // 32 or 64 KB: the ring starts 1 KB aligned
   L.w = off;
   off += stages * stage_w;
   L.s = off;
   off += stages * stage_s;
   off = (off + 15) & ~15;
   L.red = off;
-  off += kRedBufs * red_floats * 4;
+  if (!wide) off += kRedBufs * red_floats * 4;
   off = (off + 15) & ~15;
   L.bar = off;
   off += (2 * kMaxStages + 2 * kRedBufs) * 8 + 16;   // ring and buffer barriers, then the gate
@@ -275,15 +283,15 @@ struct TileCursor {
 
 // The reducer's work for one tile with more outputs than lanes: each lane sums R outputs
 // o = base + lane + 32 r at once.
-template <int R>
-__device__ __forceinline__ void reduce_tile_batched(const float* red, const PGemv& gm, int outs, int nrows, int r0,
+template <int R, class Part>
+__device__ __forceinline__ void reduce_tile_batched(const Part& P, const PGemv& gm, int outs, int nrows, int r0,
                                                     int lane) {
   for (int base = 0; base < outs; base += 32 * R) {
-    const float* rr[R];
+    int oo[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) rr[r] = red + min(base + lane + 32 * r, outs - 1) * gm.cp;
+    for (int r = 0; r < R; ++r) oo[r] = min(base + lane + 32 * r, outs - 1);
     float v[R];
-    sum_spans_batch<R>(v, rr, gm.nspan);
+    sum_spans_batch<R>(v, P, oo, gm.nspan);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       const int o = base + lane + 32 * r;
@@ -297,12 +305,12 @@ __device__ __forceinline__ void reduce_tile_batched(const float* red, const PGem
 
 // The reducer's work for one tile: each output o = m * nrows + r (batch row m, tile row r) summed
 // over its spans by Q lanes, written to y as FP16.
-template <int Q>
-__device__ __forceinline__ void reduce_tile(const float* red, const PGemv& gm, int outs, int nrows, int r0,
+template <int Q, class Part>
+__device__ __forceinline__ void reduce_tile(const Part& P, const PGemv& gm, int outs, int nrows, int r0,
                                             int lane) {
   for (int base = 0; base < outs; base += 32 / Q) {
     const int o = base + lane / Q;
-    const float v = sum_spans<Q>(red + min(o, outs - 1) * gm.cp, gm.nspan, lane % Q);
+    const float v = sum_spans<Q>(P, min(o, outs - 1), gm.nspan, lane % Q);
     if (o < outs && lane % Q == 0) {
       const int m = o / nrows;
       gm.y[(size_t)m * gm.N + r0 + (o - m * nrows)] = __float2half_rn(v);
@@ -310,13 +318,24 @@ __device__ __forceinline__ void reduce_tile(const float* red, const PGemv& gm, i
   }
 }
 
+// As many lanes per output (1, 2, 4 or 8) as make one pass over the tile's outputs.
+template <class Part>
+__device__ __forceinline__ void reduce_tile_any(const Part& P, const PGemv& gm, int outs, int nrows, int r0,
+                                                int lane) {
+  if (outs <= 4) reduce_tile<8>(P, gm, outs, nrows, r0, lane);
+  else if (outs <= 8) reduce_tile<4>(P, gm, outs, nrows, r0, lane);
+  else if (outs <= 16) reduce_tile<2>(P, gm, outs, nrows, r0, lane);
+  else reduce_tile_batched<4>(P, gm, outs, nrows, r0, lane);
+}
+
 // NSCF: the number of block scales per full span when every GEMV of the launch has the same block
 // size (1, 2 or 4), compiled in; 0 when they differ (the general unit serves every span).
-template <int KB, bool SC32, int NSCF>
+// WIDE: the 64 KB byte-pair table, with the partial sums in its gaps (batch 1 only).
+template <int KB, bool SC32, int NSCF, bool WIDE>
 __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid_constant__ PParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const PLayout Lo = playout(p.stages, p.stage_w, p.stage_s, p.red_floats);
+  const PLayout Lo = playout(p.stages, p.stage_w, p.stage_s, p.red_floats, WIDE);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lo.bar);
   uint64_t* empty = full + kMaxStages;
   uint64_t* rfull = empty + kMaxStages;
@@ -328,6 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
   const int n_cons = kConsumerWarps * 32;
   const int G = (int)gridDim.x;
   const int NS = p.stages;
+  if (WIDE && p.M != 1) {   // the gaps hold batch 1's partials only (the host never launches this)
+    if (threadIdx.x == 0) atomicCAS(&g_error_word, 0u, 0x20bu);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -415,14 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
       if (ok) ok = mbar_wait(&rfull[b], (j / kRedBufs) & 1, 0x203);
       const int r0 = (t - gm.tile0) * gm.rpt;
       const int nrows = min(gm.rpt, gm.N - r0);
-      const float* red = red_base + b * p.red_floats;
-      // output o = m * nrows + r: partials red[o * cp ... + nspan)
+      // output o = m * nrows + r (batch row m, tile row r)
       const int outs = nrows * p.M;
-      // as many lanes per output (1, 2, 4 or 8) as make one pass over the tile's outputs
-      if (outs <= 4) reduce_tile<8>(red, gm, outs, nrows, r0, lane);
-      else if (outs <= 8) reduce_tile<4>(red, gm, outs, nrows, r0, lane);
-      else if (outs <= 16) reduce_tile<2>(red, gm, outs, nrows, r0, lane);
-      else reduce_tile_batched<4>(red, gm, outs, nrows, r0, lane);
+      if (WIDE) {
+        const PartGaps P{smem + Lo.lut + kGapOffset + b * kGapBufBytes, gaps_per_output(gm.nspan)};
+        reduce_tile_any(P, gm, outs, nrows, r0, lane);
+      } else {
+        const PartDense P{red_base + b * p.red_floats, gm.cp};
+        reduce_tile_any(P, gm, outs, nrows, r0, lane);
+      }
       // the CTA's last tile of level L: publish before the cursor reads the next tile's tables
       const bool publish = p.counters && cur.level_last();
       __syncwarp();
@@ -446,9 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
 
   // ================================================================== consumer warps
   const int tid = threadIdx.x;
-  build_lut(reinterpret_cast<uint32_t*>(smem + Lo.lut), p.fmt, p.codebook, tid, n_cons);
+  build_lut(reinterpret_cast<uint32_t*>(smem + Lo.lut), p.fmt, p.codebook, tid, n_cons, WIDE);
   asm volatile("bar.sync 1, %0;" ::"r"(n_cons) : "memory");   // the table is read before the first level
-  const uint32_t lut_lane = smem_u32(smem + Lo.lut) + (uint32_t)lane * 4u;
+  // 32 KB table: the lane's entry 0; 64 KB table: the table (the lane enters through the permute)
+  const uint32_t lut_lane = smem_u32(smem + Lo.lut) + (WIDE ? 0u : (uint32_t)lane * 4u);
   constexpr int RUN = KB / 8;
   constexpr int NKB = kSpanK / KB;
   const int g = lane >> 2, tq = lane & 3;
@@ -466,8 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
       off1[jj] = (uint32_t)((((byte >> 4) ^ x1) << 4) | (byte & 15));
     }
   }
+  constexpr int DSUB = KB == 64 ? 1 : 8;   // tile row of MMA row g + 8 minus that of MMA row g
+  const int rsub = KB == 64 ? 2 * g : g;   // tile row of MMA row g within its row group
   int j = 0;
-  int ubase = 0;            // units of this CTA's earlier tiles (round-robin continues across tiles)
+  int st = 0;               // ring stage of tile j and the parity of its current round
+  uint32_t sph = 0;
+  int wrot = 0;             // the warp that takes the first chunk of the next tile
   bool ok = true;
   bool pdl_done = false;
   TileCursor cur;
@@ -476,25 +505,27 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
   for (; cur.valid(p); cur.next(p), ++j) {
     const int L = cur.L;
     const PGemv& gm = cur.gm;
-    const int st = j % NS;
-    const int b = j % kRedBufs;
+    const int b = j & 1;
     const int r0 = (cur.t - gm.tile0) * gm.rpt;
     const int nrows = min(gm.rpt, gm.N - r0);
     const int rgs = (nrows + 15) >> 4;
     const int units = rgs * gm.nspan;
-    const bool full_last = (gm.K % kSpanK) == 0;   // every span full, scale runs aligned
-    const int lgbs = 31 - __clz(gm.bs);
     const uint32_t tile_s = smem_u32(smem + Lo.w + st * p.stage_w);
     const uint32_t stile_s = smem_u32(smem + Lo.s + st * p.stage_s);
-    float* red = red_base + b * p.red_floats;
+    const uint32_t red_s = smem_u32(red_base + b * p.red_floats);
     // x of batch row g (the last batch row in lanes above the batch: those B columns are never
     // stored)
     const uint8_t* xrow = reinterpret_cast<const uint8_t*>(gm.x + (size_t)min(g, p.M - 1) * gm.K) + (KB / 2) * tq;
-    // this warp's units u = u0, u0 + 14, ... of the tile as (row group rg, span c), stepped without
-    // divisions; MMA rows g and g + 8 stand for tile rows ra and rb of the row group
-    const int u0 = (warp - ubase % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
-    int rg = u0 / gm.nspan, c = u0 - rg * gm.nspan;
-    const int rsub_a = KB == 64 ? 2 * g : g, rsub_b = rsub_a + (KB == 64 ? 1 : 8);
+    // this warp's units: a contiguous chunk of the tile's units in span-major order
+    // u = c * rgs + rg (c: span, rg: row group), so that consecutive units share x; chunk sizes
+    // differ by at most one, and the warps that take the larger ones rotate from tile to tile
+    int wq = warp - wrot;
+    if (wq < 0) wq += kConsumerWarps;
+    const int uq = units / kConsumerWarps, ur = units - uq * kConsumerWarps;
+    const int u_begin = wq * uq + min(wq, ur);
+    int left = uq + (wq < ur ? 1 : 0);
+    wrot += ur;
+    if (wrot >= kConsumerWarps) wrot -= kConsumerWarps;
     const bool is_level_end = cur.level_last() && L + 1 < p.nlevels;
     if (L != Lcur) {
       // ---- this CTA's first tile of the level: wait until this level's inputs exist
@@ -513,49 +544,72 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
       Lcur = L;
     }
     // every lane waits for itself: one instruction per warp, no broadcast round trip
-    if (ok) ok = mbar_wait(&full[st], (j / NS) & 1, 0x205);
-    if (j >= kRedBufs && ok) ok = mbar_wait(&rfree[b], ((j / kRedBufs) - 1) & 1, 0x206);
-    if (ok) {
+    if (ok) ok = mbar_wait(&full[st], sph, 0x205);
+    if (j >= kRedBufs && ok) ok = mbar_wait(&rfree[b], ((j >> 1) - 1) & 1, 0x206);
+    if (ok && left > 0) {
+      const bool full_last = (gm.K % kSpanK) == 0;   // every span full, scale runs aligned
+      const int lgbs = 31 - __clz(gm.bs);
       const int sshift = 31 - __clz(gm.bs / KB);
-      for (int u = u0; u < units; u += kConsumerWarps) {
-        const int ra = rg * 16 + rsub_a, rb = rg * 16 + rsub_b;
-        const int rac = min(ra, nrows - 1), rbc = min(rb, nrows - 1);
-        const uint32_t a0 = tile_s + (uint32_t)((c >> 1) * gm.slot + ra * 128);
-        const uint32_t a1 = tile_s + (uint32_t)((c >> 1) * gm.slot + rb * 128);
-        const uint32_t hm = (uint32_t)(c & 1) << 6;
-        uint32_t o0[NKB], o1[NKB];
-#pragma unroll
-        for (int jj = 0; jj < NKB; ++jj) { o0[jj] = off0[jj] ^ hm; o1[jj] = off1[jj] ^ hm; }
-        const uint32_t s0a = stile_s + (uint32_t)(rac * gm.srb), s1a = stile_s + (uint32_t)(rbc * gm.srb);
+      // first unit of the chunk: u_begin / rgs, exact in FP32 (u_begin < 2^11, rgs <= 16)
+      int c = (int)(((float)u_begin + 0.5f) * __frcp_rn((float)rgs));
+      int rg = u_begin - c * rgs;
+      if (rg < 0) { --c; rg += rgs; }        // never taken (the quotient is exact); keeps 0 <= rg < rgs
+      if (rg >= rgs) { ++c; rg -= rgs; }
+      // partial-sum rows of batch rows 2t and 2t + 1 (stored only where those rows exist)
+      const bool m0 = 2 * tq < p.M, m1 = 2 * tq + 1 < p.M;
+      const uint32_t pm0 = red_s + (uint32_t)(2 * tq * nrows * gm.cp) * 4u;
+      const uint32_t pm1 = pm0 + (uint32_t)(nrows * gm.cp) * 4u;
+      const uint32_t pdsub = (uint32_t)(DSUB * gm.cp) * 4u;
+      // gaps (batch 1): output r's span c at gap r * hpo + c / 32, word (c + 4 (r & 7)) mod 32
+      const int hpo = gaps_per_output(gm.nspan);
+      const uint32_t gap_s = smem_u32(smem + Lo.lut + kGapOffset + b * kGapBufBytes);
+      const int rot_a = 4 * (rsub & 7), rot_b = 4 * ((rsub + DSUB) & 7);   // r & 7 of rows ra, rb
+      while (left > 0) {
+        // ---- span c: x, its box and half, its scale column
+        uint32_t xr[NKB][KB / 8];
         const uint8_t* xg = xrow + c * (kSpanK * 2);
+        const int nkb = min(kSpanK, gm.K - c * kSpanK) / KB;
         const int sidx0 = (c * kSpanK) >> lgbs;
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        const bool v0 = ra < nrows, v1 = rb < nrows;
-        if (NSCF > 0 && full_last) {
-          // every span full, each row's span scales one aligned vector: NSCF = max(1, 128 / bs)
-          const uint32_t so = (uint32_t)(sidx0 * (SC32 ? 4 : 2));
-          mma_unit<KB, SC32, NSCF>(acc, a0, a1, o0, o1, s0a + so, s1a + so, v0, v1, xg, 0, 0, 0, lut_lane, lane);
-        } else {
-          const int nkb = min(kSpanK, gm.K - c * kSpanK) / KB;
-          mma_unit<KB, SC32, 0>(acc, a0, a1, o0, o1, s0a, s1a, v0, v1, xg, sidx0, sshift, nkb, lut_lane, lane);
-        }
-        // partials: batch rows 2t, 2t + 1 of weight rows ra and rb
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int m = 2 * tq + q;
-          if (m < p.M) {
-            if (ra < nrows) red[(m * nrows + ra) * gm.cp + c] = acc[q];
-            if (rb < nrows) red[(m * nrows + rb) * gm.cp + c] = acc[2 + q];
+        if (NSCF > 0 && full_last) load_span_x<KB, true>(xr, xg, NKB);
+        else load_span_x<KB, false>(xr, xg, nkb);
+        const uint32_t bc = tile_s + (uint32_t)((c >> 1) * gm.slot + rsub * 128) + ((uint32_t)(c & 1) << 6);
+        const uint32_t sc = stile_s + (uint32_t)(NSCF > 0 && full_last ? sidx0 * (SC32 ? 4 : 2) : 0);
+        const uint32_t ga = gap_s + (uint32_t)(((c >> 5) << 8) + ((((c & 31) + rot_a) & 31) << 2));
+        const uint32_t gb = gap_s + (uint32_t)(((c >> 5) << 8) + ((((c & 31) + rot_b) & 31) << 2)) +
+                            (uint32_t)(DSUB * hpo * 256);
+        const int cnt = min(left, rgs - rg);
+        for (int i = 0; i < cnt; ++i, ++rg) {
+          const int ra = rg * 16 + rsub, rb = ra + DSUB;
+          const uint32_t b0 = bc + (uint32_t)rg * 2048u, b1 = b0 + DSUB * 128u;
+          const uint32_t s0a = sc + (uint32_t)(min(ra, nrows - 1) * gm.srb);
+          const uint32_t s1a = sc + (uint32_t)(min(rb, nrows - 1) * gm.srb);
+          float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if (NSCF > 0 && full_last) {
+            // every span full, each row's span scales one aligned vector: NSCF = max(1, 128 / bs)
+            mma_unit<KB, SC32, NSCF, WIDE>(acc, b0, b1, off0, off1, s0a, s1a, xr, 0, 0, 0, lut_lane, lane);
+          } else {
+            mma_unit<KB, SC32, 0, WIDE>(acc, b0, b1, off0, off1, s0a, s1a, xr, sidx0, sshift, nkb, lut_lane, lane);
+          }
+          const bool va = ra < nrows, vb = rb < nrows;
+          if (WIDE) {
+            // batch 1: batch row 0 of weight rows ra and rb (lanes t = 0)
+            const uint32_t go = (uint32_t)(ra * hpo) << 8;
+            sts_f32_if(ga + go, acc[0], m0 && va);
+            sts_f32_if(gb + go, acc[2], m0 && vb);
+          } else {
+            // partials: batch rows 2t, 2t + 1 of weight rows ra and rb, at red[(m * nrows + r) * cp + c]
+            const uint32_t o = (uint32_t)(ra * gm.cp + c) * 4u;
+            sts_f32_if(pm0 + o, acc[0], m0 && va);
+            sts_f32_if(pm0 + o + pdsub, acc[2], m0 && vb);
+            sts_f32_if(pm1 + o, acc[1], m1 && va);
+            sts_f32_if(pm1 + o + pdsub, acc[3], m1 && vb);
           }
         }
-        c += kConsumerWarps;
-        while (c >= gm.nspan) {
-          c -= gm.nspan;
-          ++rg;
-        }
+        left -= cnt;
+        rg = 0;
+        ++c;
       }
     }
-    ubase += units;
     __syncwarp();
     if (lane == 0) {
       // the CTA's last tile of a level: close the stream gate before this stage is released, so
@@ -564,6 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
       if (p.counters && is_level_end) *gate = 0;
       mbar_arrive(&empty[st]);
       mbar_arrive(&rfull[b]);
+    }
+    if (++st == NS) {
+      st = 0;
+      sph ^= 1u;
     }
   }
   asm volatile("bar.sync 2, %0;" ::"r"(n_cons + 32) : "memory");
@@ -617,8 +675,9 @@ struct Job {
   int N, K, bs, level;
 };
 
-// Rows per tile and its constraints for one GEMV at a stage budget (bytes of packed data).
-static void tile_rows(int fmt, int M, int K, int bs, int stage_target, GeomG& o) {
+// Rows per tile and its constraints for one GEMV at a stage budget (bytes of packed data).  wide:
+// the partial sums live in the 64 KB table's gaps (batch 1), which bounds the rows of a tile.
+static void tile_rows(int fmt, int M, int K, int bs, int stage_target, bool wide, GeomG& o) {
   o.nspan = span_count(K);
   o.nbox = box_count(K);
   o.cp = part_stride(o.nspan);
@@ -628,6 +687,10 @@ static void tile_rows(int fmt, int M, int K, int bs, int stage_target, GeomG& o)
   if (rows > 16) rows &= ~15;                   // whole MMA row groups when the tile has several
   rows = max(1, min(rows, kMaxRowsPerTile));
   while (rows > 1 && rows * M * o.cp > kRedCapFloats) rows = rows > 16 ? rows - 16 : rows - 1;
+  if (wide) {
+    const int cap = kGapsPerBuf / gaps_per_output(o.nspan);   // outputs per gap buffer (M = 1)
+    while (rows > 1 && rows > cap) rows = rows > 16 ? rows - 16 : rows - 1;
+  }
   rows = (rows / o.align_rows) * o.align_rows;
   if (rows < o.align_rows) rows = o.align_rows;
   o.rpt_max = rows;
@@ -636,6 +699,7 @@ static void tile_rows(int fmt, int M, int K, int bs, int stage_target, GeomG& o)
 
 struct Plan {
   int stage_target, stages, stage_w, stage_s, red_floats, kb;
+  bool wide;   // 64 KB table, partial sums in its gaps
   PLayout L;
 };
 
@@ -643,8 +707,9 @@ struct Plan {
 // the fixed parts, then as many ring stages (2 ... kMaxStages) as shared memory holds; the stage
 // size steps down from kStageTarget until two stages fit.  All GEMVs must share the k-block
 // width (scale blocks of 32, or of 64 and more).
-static bool plan_layout(int fmt, int M, const Job* jobs, int n, Plan& P) {
+static bool plan_layout_with(int fmt, int M, const Job* jobs, int n, bool wide, Plan& P) {
   P.kb = kb_of(jobs[0].bs);
+  P.wide = wide;
   for (int i = 0; i < n; ++i)
     if (kb_of(jobs[i].bs) != P.kb || !shape_ok(jobs[i].K, jobs[i].bs)) return false;
   for (P.stage_target = kStageTarget; P.stage_target >= 2048; P.stage_target = P.stage_target * 3 / 4) {
@@ -652,8 +717,9 @@ static bool plan_layout(int fmt, int M, const Job* jobs, int n, Plan& P) {
     bool fits = true;
     for (int i = 0; i < n && fits; ++i) {
       GeomG gg;
-      tile_rows(fmt, M, jobs[i].K, jobs[i].bs, P.stage_target, gg);
+      tile_rows(fmt, M, jobs[i].K, jobs[i].bs, P.stage_target, wide, gg);
       if (gg.red_need > kRedCapFloats) fits = false;
+      if (wide && gg.rpt_max * gaps_per_output(gg.nspan) > kGapsPerBuf) fits = false;
       P.stage_w = max(P.stage_w, stage_bytes(gg.nbox, gg.rpt_max));
       P.stage_s = max(P.stage_s, ((gg.rpt_max * gg.srb) + 15) & ~15);
       P.red_floats = max(P.red_floats, gg.red_need);
@@ -661,11 +727,31 @@ static bool plan_layout(int fmt, int M, const Job* jobs, int n, Plan& P) {
     if (!fits) continue;
     P.red_floats = (P.red_floats + kRedSlackFloats + 3) & ~3;
     for (P.stages = kMaxStages; P.stages >= 2; --P.stages) {
-      P.L = playout(P.stages, P.stage_w, P.stage_s, P.red_floats);
+      P.L = playout(P.stages, P.stage_w, P.stage_s, P.red_floats, wide);
       if (P.L.total + 1024 <= kSmemCap) return true;   // + the 1 KB alignment slack
     }
   }
   return false;
+}
+
+// The 64 KB table at batch 1 when it leaves the same stage budget as the 32 KB table (its gaps
+// take the partial sums), else the 32 KB table.
+static bool plan_layout(int fmt, int M, const Job* jobs, int n, Plan& P) {
+  if (M == 1) {
+    Plan W, N;
+    const bool w_ok = plan_layout_with(fmt, M, jobs, n, true, W);
+    const bool n_ok = plan_layout_with(fmt, M, jobs, n, false, N);
+    if (w_ok && (!n_ok || (W.stage_target >= N.stage_target && W.stages >= 2))) {
+      P = W;
+      return true;
+    }
+    if (n_ok) {
+      P = N;
+      return true;
+    }
+    return false;
+  }
+  return plan_layout_with(fmt, M, jobs, n, false, P);
 }
 
 int simt_max_batch(int format, int K, int bs) {
@@ -730,7 +816,7 @@ static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* 
     int rmin = 1 << 30;
     while (i < n && jobs[i].level == Lv) {
       GeomG gg;
-      tile_rows(fmt, M, jobs[i].K, jobs[i].bs, P.plan.stage_target, gg);
+      tile_rows(fmt, M, jobs[i].K, jobs[i].bs, P.plan.stage_target, P.plan.wide, gg);
       rows += jobs[i].N;
       rmin = min(rmin, gg.rpt_max);
       ++i;
@@ -742,7 +828,7 @@ static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* 
     const long long tpc = (rows + (long long)gmax * rmin - 1) / ((long long)gmax * rmin);
     for (int q = first; q < i; ++q) {
       GeomG gg;
-      tile_rows(fmt, M, jobs[q].K, jobs[q].bs, P.plan.stage_target, gg);
+      tile_rows(fmt, M, jobs[q].K, jobs[q].bs, P.plan.stage_target, P.plan.wide, gg);
       int rpt = (int)((rows + (long long)gmax * tpc - 1) / ((long long)gmax * tpc));
       if (rpt > 16) rpt = (rpt + 15) & ~15;                          // whole MMA row groups
       rpt = ((rpt + gg.align_rows - 1) / gg.align_rows) * gg.align_rows;
@@ -766,9 +852,9 @@ static cudaError_t prepare(int fmt, const Job* jobs, int n, int M, const float* 
   return cudaSuccess;
 }
 
-template <int KB, bool SC32, int NSCF>
+template <int KB, bool SC32, int NSCF, bool WIDE>
 static cudaError_t launch_prepared(Prepared& P, unsigned* counters, bool pdl, cudaStream_t stream) {
-  auto kern = w4_persistent_kernel<KB, SC32, NSCF>;
+  auto kern = w4_persistent_kernel<KB, SC32, NSCF, WIDE>;
   static FuncAttrCache attrs;   // one per instance
   cudaError_t ea = attrs.ensure([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemCap); });
   if (ea != cudaSuccess) return ea;
@@ -792,25 +878,31 @@ static cudaError_t launch_prepared(Prepared& P, unsigned* counters, bool pdl, cu
   return e;
 }
 
-// The instance for the launch's format, k-block width and scales per span (0 when the GEMVs' block
-// sizes differ).
-static cudaError_t dispatch(int fmt, Prepared& P, unsigned* counters, bool pdl, cudaStream_t s) {
+// The instance for the launch's format, k-block width, scales per span (0 when the GEMVs' block
+// sizes differ) and table.
+template <bool WIDE>
+static cudaError_t dispatch_table(int fmt, Prepared& P, unsigned* counters, bool pdl, cudaStream_t s) {
   int bs = P.gm[0].bs;
   for (const PGemv& g : P.gm)
     if (g.bs != bs) bs = 0;
   const int nsc = bs == 0 ? 0 : (bs >= kSpanK ? 1 : kSpanK / bs);
   if (P.plan.kb == 32) {   // block size 32: four scales per span
-    if (fmt == 0) return launch_prepared<32, true, 4>(P, counters, pdl, s);
-    return launch_prepared<32, false, 4>(P, counters, pdl, s);
+    if (fmt == 0) return launch_prepared<32, true, 4, WIDE>(P, counters, pdl, s);
+    return launch_prepared<32, false, 4, WIDE>(P, counters, pdl, s);
   }
   if (fmt == 0) {
-    if (nsc == 2) return launch_prepared<64, true, 2>(P, counters, pdl, s);
-    if (nsc == 1) return launch_prepared<64, true, 1>(P, counters, pdl, s);
-    return launch_prepared<64, true, 0>(P, counters, pdl, s);
+    if (nsc == 2) return launch_prepared<64, true, 2, WIDE>(P, counters, pdl, s);
+    if (nsc == 1) return launch_prepared<64, true, 1, WIDE>(P, counters, pdl, s);
+    return launch_prepared<64, true, 0, WIDE>(P, counters, pdl, s);
   }
-  if (nsc == 2) return launch_prepared<64, false, 2>(P, counters, pdl, s);
-  if (nsc == 1) return launch_prepared<64, false, 1>(P, counters, pdl, s);
-  return launch_prepared<64, false, 0>(P, counters, pdl, s);
+  if (nsc == 2) return launch_prepared<64, false, 2, WIDE>(P, counters, pdl, s);
+  if (nsc == 1) return launch_prepared<64, false, 1, WIDE>(P, counters, pdl, s);
+  return launch_prepared<64, false, 0, WIDE>(P, counters, pdl, s);
+}
+
+static cudaError_t dispatch(int fmt, Prepared& P, unsigned* counters, bool pdl, cudaStream_t s) {
+  if (P.plan.wide) return dispatch_table<true>(fmt, P, counters, pdl, s);
+  return dispatch_table<false>(fmt, P, counters, pdl, s);
 }
 
 cudaError_t launch_gemv_simt(int format, const uint8_t* packed, const void* scales, const float* codebook,
