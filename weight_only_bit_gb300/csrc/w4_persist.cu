@@ -54,6 +54,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include <cuda_fp16.h>
@@ -564,50 +565,57 @@ __global__ void __launch_bounds__(kThreads, 1) w4_persistent_kernel(const __grid
       const int hpo = gaps_per_output(gm.nspan);
       const uint32_t gap_s = smem_u32(smem + Lo.lut + kGapOffset + b * kGapBufBytes);
       const int rot_a = 4 * (rsub & 7), rot_b = 4 * ((rsub + DSUB) & 7);   // r & 7 of rows ra, rb
-      while (left > 0) {
-        // ---- span c: x, its box and half, its scale column
-        uint32_t xr[NKB][KB / 8];
-        const uint8_t* xg = xrow + c * (kSpanK * 2);
-        const int nkb = min(kSpanK, gm.K - c * kSpanK) / KB;
-        const int sidx0 = (c * kSpanK) >> lgbs;
-        if (NSCF > 0 && full_last) load_span_x<KB, true>(xr, xg, NKB);
-        else load_span_x<KB, false>(xr, xg, nkb);
-        const uint32_t bc = tile_s + (uint32_t)((c >> 1) * gm.slot + rsub * 128) + ((uint32_t)(c & 1) << 6);
-        const uint32_t sc = stile_s + (uint32_t)(NSCF > 0 && full_last ? sidx0 * (SC32 ? 4 : 2) : 0);
-        const uint32_t ga = gap_s + (uint32_t)(((c >> 5) << 8) + ((((c & 31) + rot_a) & 31) << 2));
-        const uint32_t gb = gap_s + (uint32_t)(((c >> 5) << 8) + ((((c & 31) + rot_b) & 31) << 2)) +
-                            (uint32_t)(DSUB * hpo * 256);
-        const int cnt = min(left, rgs - rg);
-        for (int i = 0; i < cnt; ++i, ++rg) {
-          const int ra = rg * 16 + rsub, rb = ra + DSUB;
-          const uint32_t b0 = bc + (uint32_t)rg * 2048u, b1 = b0 + DSUB * 128u;
-          const uint32_t s0a = sc + (uint32_t)(min(ra, nrows - 1) * gm.srb);
-          const uint32_t s1a = sc + (uint32_t)(min(rb, nrows - 1) * gm.srb);
-          float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          if (NSCF > 0 && full_last) {
-            // every span full, each row's span scales one aligned vector: NSCF = max(1, 128 / bs)
-            mma_unit<KB, SC32, NSCF, WIDE>(acc, b0, b1, off0, off1, s0a, s1a, xr, 0, 0, 0, lut_lane, lane);
-          } else {
-            mma_unit<KB, SC32, 0, WIDE>(acc, b0, b1, off0, off1, s0a, s1a, xr, sidx0, sshift, nkb, lut_lane, lane);
+      // the chunk's units; FULL: every span full, each row's span scales one aligned vector
+      // (NSCF = max(1, 128 / bs)), decided once per tile
+      auto run_chunk = [&](auto full_tag) {
+        constexpr bool FULL = decltype(full_tag)::value;
+        constexpr int NSC = FULL ? NSCF : 0;
+        while (left > 0) {
+          // ---- span c: x, its box and half, its scale column
+          uint32_t xr[NKB][KB / 8];
+          const uint8_t* xg = xrow + c * (kSpanK * 2);
+          const int nkb = min(kSpanK, gm.K - c * kSpanK) / KB;
+          const int sidx0 = (c * kSpanK) >> lgbs;
+          load_span_x<KB, FULL>(xr, xg, nkb);
+          const uint32_t bc = tile_s + (uint32_t)((c >> 1) * gm.slot + rsub * 128) + ((uint32_t)(c & 1) << 6);
+          const uint32_t sc = stile_s + (uint32_t)(FULL ? sidx0 * (SC32 ? 4 : 2) : 0);
+          const uint32_t ga = gap_s + (uint32_t)(((c >> 5) << 8) + ((((c & 31) + rot_a) & 31) << 2));
+          const uint32_t gb = gap_s + (uint32_t)(((c >> 5) << 8) + ((((c & 31) + rot_b) & 31) << 2)) +
+                              (uint32_t)(DSUB * hpo * 256);
+          const int cnt = min(left, rgs - rg);
+          for (int i = 0; i < cnt; ++i, ++rg) {
+            const int ra = rg * 16 + rsub, rb = ra + DSUB;
+            const uint32_t b0 = bc + (uint32_t)rg * 2048u, b1 = b0 + DSUB * 128u;
+            const uint32_t s0a = sc + (uint32_t)(min(ra, nrows - 1) * gm.srb);
+            const uint32_t s1a = sc + (uint32_t)(min(rb, nrows - 1) * gm.srb);
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            mma_unit<KB, SC32, NSC, WIDE>(acc, b0, b1, off0, off1, s0a, s1a, xr, FULL ? 0 : sidx0, sshift, nkb,
+                                          lut_lane, lane);
+            const bool va = ra < nrows, vb = rb < nrows;
+            if (WIDE) {
+              // batch 1: batch row 0 of weight rows ra and rb (lanes t = 0)
+              const uint32_t go = (uint32_t)(ra * hpo) << 8;
+              sts_f32_if(ga + go, acc[0], m0 && va);
+              sts_f32_if(gb + go, acc[2], m0 && vb);
+            } else {
+              // partials: batch rows 2t, 2t + 1 of weight rows ra and rb, at red[(m * nrows + r) * cp + c]
+              const uint32_t o = (uint32_t)(ra * gm.cp + c) * 4u;
+              sts_f32_if(pm0 + o, acc[0], m0 && va);
+              sts_f32_if(pm0 + o + pdsub, acc[2], m0 && vb);
+              sts_f32_if(pm1 + o, acc[1], m1 && va);
+              sts_f32_if(pm1 + o + pdsub, acc[3], m1 && vb);
+            }
           }
-          const bool va = ra < nrows, vb = rb < nrows;
-          if (WIDE) {
-            // batch 1: batch row 0 of weight rows ra and rb (lanes t = 0)
-            const uint32_t go = (uint32_t)(ra * hpo) << 8;
-            sts_f32_if(ga + go, acc[0], m0 && va);
-            sts_f32_if(gb + go, acc[2], m0 && vb);
-          } else {
-            // partials: batch rows 2t, 2t + 1 of weight rows ra and rb, at red[(m * nrows + r) * cp + c]
-            const uint32_t o = (uint32_t)(ra * gm.cp + c) * 4u;
-            sts_f32_if(pm0 + o, acc[0], m0 && va);
-            sts_f32_if(pm0 + o + pdsub, acc[2], m0 && vb);
-            sts_f32_if(pm1 + o, acc[1], m1 && va);
-            sts_f32_if(pm1 + o + pdsub, acc[3], m1 && vb);
-          }
+          left -= cnt;
+          rg = 0;
+          ++c;
         }
-        left -= cnt;
-        rg = 0;
-        ++c;
+      };
+      if constexpr (NSCF > 0) {
+        if (full_last) run_chunk(std::true_type{});
+        else run_chunk(std::false_type{});
+      } else {
+        run_chunk(std::false_type{});
       }
     }
     __syncwarp();
