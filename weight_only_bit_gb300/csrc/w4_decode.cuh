@@ -3,7 +3,8 @@
 // The decode is a 256-entry table indexed by a whole packed byte that returns both nibbles' values
 // (FP16) as one half2, element 2j in the low half ("LLM Quantization on RTX 4060", section "Kernel
 // Implementation": the high nibble of byte j is element 2j); one copy of the table per lane, entry
-// b of lane l at word b * 32 + l, so any pattern of bytes across a warp is conflict-free.
+// b of lane l at word b * 32 + l (or b * 64 + l in the 64 KB layout), so any pattern of bytes
+// across a warp is conflict-free.
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>

@@ -25,8 +25,11 @@
 //     the swizzled loads conflict-free); each byte is one A-fragment register, two
 //     consecutive k of one row, decoded by one shared-memory lookup in a byte-pair table (NF4 code
 //     values, q - 8 for INT4, E2M1 values for FP4, all exact in FP16 except the NF4 code values,
-//     which are rounded to FP16).  K is permuted identically in A and B, so the B fragment is the
-//     lane's own x elements, loaded in natural order;
+//     which are rounded to FP16).  At batch 1 the table is 64 KB (entries 256 bytes apart, so one
+//     byte permute forms a lookup's offset from the packed byte and the lane, and the table's
+//     address folds into the load) and its free halves hold the partial sums; above batch 1 it is
+//     32 KB (one shift-add per lookup).  K is permuted identically in A and B, so the B fragment is
+//     the lane's own x elements, loaded in natural order;
 //   * the MMAs of one scale block start from zero, and the block's scale (FP32 absmax for NF4,
 //     FP16 scale for INT4 and FP4) multiplies the result into the unit's FP32 accumulators;
 //   * each unit leaves one FP32 partial per (batch row, weight row, span) in shared memory, and the
@@ -43,9 +46,10 @@
 //     level's completion is published and the next level waits slows that release and its polls.
 //     The consumers open the gate before they wait for a level's first tile, so a tile held back
 //     at a level's end is issued as soon as the level starts;
-//   * 14 consumer warps (16 warps in all, so each thread may hold 128 registers): the units of
-//     each tile, round-robin over the warps (continuing across tiles, so an uneven tile does not
-//     always load the same warps);
+//   * 14 consumer warps (16 warps in all, so each thread may hold 128 registers): each takes a
+//     contiguous chunk of the tile's units in span-major order (consecutive units of a warp share a
+//     span, so its x stays in registers while the row group advances); chunk sizes differ by at
+//     most one and the warps that take the larger ones rotate from tile to tile;
 //   * reducer warp: sums each row's partials, writes y, and after the CTA's last tile of a level
 //     publishes completion with one release, before it reads any table entry of the next tile
 //     (whether a tile ends the CTA's part of a level is known from the cursor alone).
