@@ -196,6 +196,12 @@ GEMV_CASES = [
     ("fp4", 2, 333, 1536, 32), ("fp4", 3, 64, 8960, 32), ("fp4", 4, 1000, 1536, 32), ("fp4", 8, 777, 1536, 32),
     ("fp4", 8, 61, 8960, 32), ("fp4", 1, 70, 512, 64), ("fp4", 2, 70, 1024, 128), ("fp4", 1, 45, 96, 32),
     ("fp4", 3, 40, 160, 32), ("fp4", 5, 129, 1536, 256),
+    # batch 1 keeps a tile's partial sums in the 64 KB table's 128-byte gaps (32 spans each): a
+    # row's spans filling one gap exactly (K 4096), spilling into a second (K 4224, also an odd
+    # box count), three gaps at the largest K, and tiles capped at 128 rows by the gaps (K 512,
+    # more rows than 152 tiles of 128)
+    ("nf4", 1, 300, 4096, 64), ("nf4", 1, 300, 4224, 64), ("fp4", 1, 257, 4224, 32),
+    ("int4", 1, 200, 10240, 128), ("nf4", 1, 40000, 512, 64),
 ]
 
 
