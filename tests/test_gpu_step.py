@@ -226,3 +226,51 @@ def test_chained_levels_read_previous_outputs(dev, fmt, batch):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert torch.all(workspace[: len(descs) + 1] == 0)          # the level counters
     w4.check(w4.w4_step_destroy(h))
+
+
+@pytest.mark.parametrize("batch", [1, 3])
+def test_step_with_mixed_block_sizes(dev, batch):
+    """GEMVs with different NF4 block sizes (64, 128, 256) and a K that is not a multiple of 128 in
+    one persistent launch: the general unit (scales looked up per k block) serves every span, and
+    the results equal the oracle and, bit for bit, one launch per GEMV (each of which compiles its
+    block size in)."""
+    code = oracle.nf4_codebook()
+    codebook = torch.tensor(code, dtype=torch.float32, device=dev)
+    # (N, K, blocksize, level)
+    shapes = [(1536, 1536, 64, 0), (700, 1536, 128, 0), (300, 1600, 64, 1), (900, 1024, 256, 2)]
+    descs, ws, xs, ys = [], [], [], []
+    for i, (n, k, bs, lev) in enumerate(shapes):
+        w = synth.weights(6100 + i, n, k, outlier_frac=0.001)
+        x = synth.activations(6200 + i, batch, k)
+        p = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
+        s = torch.empty((n, k // bs), dtype=torch.float32, device=dev)
+        w4.check(w4.w4_quantize_nf4(torch.from_numpy(w).to(dev), p, s, codebook, n, k, bs))
+        X = torch.from_numpy(x).to(dev)
+        y = torch.full((batch, n), float("nan"), dtype=torch.float16, device=dev)
+        ws.append(w); xs.append(X); ys.append(y)
+        descs.append(dict(format=w4._lib.W4_FMT_NF4, packed=p, scales=s, codebook=codebook, x=X, y=y,
+                          M=batch, N=n, K=k, blocksize=bs, level=lev))
+    torch.cuda.synchronize()
+    workspace = torch.zeros(w4.w4_step_workspace_bytes(len(descs)) // 4, dtype=torch.int32, device=dev)
+    st, h = w4.w4_step_create(descs, workspace)
+    w4.check(st, "step create")
+    stream = torch.cuda.Stream(dev)
+    w4.check(w4.w4_step_launch(h, stream))
+    torch.cuda.synchronize()
+    assert w4.w4_device_check(stream) == 0
+    got = [y.clone() for y in ys]
+    for i, (n, k, bs, lev) in enumerate(shapes):
+        p, s = oracle.quantize_nf4(ws[i], code, bs)
+        y_ref = oracle.gemv_nf4(p, s, code, xs[i].cpu().numpy().astype(np.float64), bs)
+        y = got[i].cpu().numpy().astype(np.float64)
+        rms = np.sqrt(np.mean(y_ref ** 2, axis=1, keepdims=True))
+        assert np.all(np.abs(y - y_ref) <= 2e-2 * rms), i
+        rel = np.linalg.norm(y - y_ref, axis=1) / np.linalg.norm(y_ref, axis=1)
+        assert np.all(rel <= 1e-3), (i, rel)
+    for y in ys:
+        y.fill_(float("nan"))
+    w4.check(w4.w4_gemv_sequence(descs, stream))
+    torch.cuda.synchronize()
+    for a, b in zip(got, ys):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    w4.check(w4.w4_step_destroy(h))
