@@ -128,6 +128,23 @@ def test_plan_batches_up_to_8_stay_on_the_small_batch_kernel(libw4, fmt, bs):
             assert p["cluster"] == 1 and p["smem_bytes"] <= 227 * 1024 and p["stages"] >= 2
 
 
+@pytest.mark.parametrize("fmt,bs", [(w4.W4_FMT_NF4, 64), (w4.W4_FMT_INT4, 128), (w4.W4_FMT_FP4, 32)])
+def test_plan_batch_1_every_k_fits(libw4, fmt, bs):
+    # batch 1 takes the 64 KB byte-pair table with the partial sums in its gaps wherever the ring
+    # keeps its stage budget: every K up to the limit must still give a launch within the shared
+    # memory of one CTA, with at least two ring stages, and the decode shapes must get the table
+    # (more than 64 KB of shared memory beside their ring stages)
+    for k in range(max(bs, 64), w4.W4_MAX_K + 1, 64):
+        if k % bs:
+            continue
+        for n in (1, 300, 40000, 151936):
+            p = _plan(fmt, 1, n, k, bs)
+            assert p["kernel"] == w4.W4_KERNEL_SMALL_BATCH and p["launches"] == 1
+            assert p["smem_bytes"] <= 227 * 1024 and p["stages"] >= 2, (k, n, p)
+    for n, k in DECODE.values():
+        assert _plan(fmt, 1, n, k, bs)["smem_bytes"] > 64 * 1024 + 2 * 8 * 1024
+
+
 @pytest.mark.parametrize("fmt,bs", [(w4.W4_FMT_NF4, 64), (w4.W4_FMT_INT4, 128), (w4.W4_FMT_NF4, 32),
                                     (w4.W4_FMT_INT4, 256), (w4.W4_FMT_FP4, 32)])
 def test_plan_tcgen05_resources(libw4, fmt, bs):
